@@ -1,0 +1,281 @@
+/*
+ * w4a16_oracle.c -- plain, slow, obviously-correct CPU oracle for group-wise
+ * asymmetric INT4 weight-only quantization and the W4A16 matmul that consumes it.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC (see oracle.py).
+ * The fp32 steps below rely on IEEE binary32 arithmetic with round-to-nearest-even
+ * (SSE on x86-64, no excess precision) and on rintf() under FE_TONEAREST, which
+ * rounds halves to even.
+ *
+ * Where each step comes from (page titles of the source pages):
+ *   - "From-Scratch INT4 Weight-Only Quantizer with Per-Group Scales and
+ *     Zero-Points", section "Architecture Overview" (item 3: per-group min/max,
+ *     scale = (max-min)/15, zero_point = round(-min/scale) clipped to [0,15]) and
+ *     "Step 5"/"Step 6" (the min/max reduction and the scale/zero-point formulas).
+ *   - "From Scratch: Building a GPTQ INT4 Quantizer in Pure Python", "Step 2"
+ *     (q = clip(round(t/scale + zero_point), 0, 15)) and "Step 4"
+ *     (dequantize = (q - zero_point) * scale).
+ *   - "Build a GPTQ INT4 Quantization Engine in Python/NumPy", "Step 4" (two
+ *     values per byte, column 2j in the low nibble, 2j+1 in the high nibble) and
+ *     "Step 5" (the dequantize-matmul y = x @ W_dequant^T, computed over chunks
+ *     of output rows so only a chunk of W is ever dequantized at once).
+ *   The fixed convention on top of those pages: groups are 128 contiguous
+ *   elements along K of W[N,K]; scale in fp32 (1 if max == min); IEEE fp32
+ *   division; round half to even; scales stored as fp16, zero-points as uint8;
+ *   dequantization uses the stored fp16 scale.
+ *
+ * Readings taken where the pages are silent or disagree (listed in the design doc):
+ *   - q and zp are computed with the fp32 scale; only dequantization uses the
+ *     stored fp16 scale.
+ *   - q = clip(rint(w / s) + zp, 0, 15), i.e. rounding happens before adding zp
+ *     (the pure-Python GPTQ page), not rint((w - min) / s).
+ *   - Inputs are finite with a finite range; nothing here checks NaN/Inf.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#include <stdlib.h>
+
+#define ORACLE_GROUP 128
+
+/* ---- IEEE binary16 <-> binary32, written from the format definition ---------
+ * binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal:    (-1)^s * 2^(e-15) * (1 + f/1024),   1 <= e <= 30
+ * Subnormal: (-1)^s * 2^(-14)  * (f/1024),       e == 0
+ * e == 31 is Inf/NaN (outside the oracle's contract, mapped to Inf/NaN anyway). */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);            /* f/1024 * 2^-14 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)f, e - 25); /* (1 + f/1024) * 2^(e-15) */
+    if (sign) v = -v;
+    return (float)v;                            /* exact: binary16 fits in binary32 */
+}
+
+/* Round a binary32 value to the nearest binary16, ties to even.  Done on the
+ * exact real value: find the binary16 spacing (quantum) at |x|, divide, round
+ * the quotient half-to-even with rint(), multiply back.  All double steps are
+ * exact because |x| has at most 24 significant bits and the quantum is a power
+ * of two. */
+uint16_t oracle_f32_to_f16_bits(float xf)
+{
+    double x = (double)xf;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(a)) return 0x7e00;
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);                     /* a = m * 2^e2, m in [0.5,1) -> floor(log2 a) = e2-1 */
+    int E = e2 - 1;
+    if (E < -14) E = -14;              /* subnormal range shares the 2^-14 binade spacing */
+    double quantum = ldexp(1.0, E - 10);
+    double n = rint(a / quantum);      /* integer count of quanta, ties to even */
+    double r = n * quantum;
+    if (r >= 65520.0 || isinf(a))      /* 65520 = max finite + half ulp: rounds to Inf */
+        return sign | 0x7c00;
+    /* re-encode r, which is exactly representable in binary16 */
+    if (r < ldexp(1.0, -14)) {
+        return sign | (uint16_t)(r / ldexp(1.0, -24));
+    }
+    int er;
+    double mr = frexp(r, &er);          /* r = mr * 2^er, mr in [0.5,1) */
+    int ebits = (er - 1) + 15;
+    uint16_t fbits = (uint16_t)((mr * 2.0 - 1.0) * 1024.0);
+    return sign | (uint16_t)(ebits << 10) | fbits;
+}
+
+/* bfloat16 is the high half of a binary32 pattern: widening is a 16-bit shift. */
+double oracle_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ---- quantize one group ---------------------------------------------------- */
+/* w: the group's values already widened (exactly) to binary32. */
+static void quantize_group(const float *w, int G, uint8_t *q, float *scale, int *zero)
+{
+    /* min/max over the group (linear scan). */
+    float mn = w[0], mx = w[0];
+    for (int i = 1; i < G; ++i) {
+        if (w[i] < mn) mn = w[i];
+        if (w[i] > mx) mx = w[i];
+    }
+    /* scale = (max - min) / 15 in fp32; a constant group gets scale 1. */
+    float s;
+    if (mx == mn) {
+        s = 1.0f;
+    } else {
+        float d = mx - mn;          /* fp32 subtraction */
+        s = d / 15.0f;              /* IEEE fp32 division */
+    }
+    /* zero-point = clip(round_half_even(-min / scale), 0, 15); the clamp is done in
+     * float so a huge quotient cannot overflow an int. */
+    float negmn = -mn;
+    float zq = rintf(negmn / s);
+    float zc = fminf(fmaxf(zq, 0.0f), 15.0f);
+    int zp = (int)zc;
+    /* q = clip(round_half_even(w / scale) + zp, 0, 15). */
+    for (int i = 0; i < G; ++i) {
+        float t = rintf(w[i] / s) + (float)zp;
+        float c = fminf(fmaxf(t, 0.0f), 15.0f);
+        q[i] = (uint8_t)(int)c;
+    }
+    *scale = s;
+    *zero = zp;
+}
+
+/* Quantize and pack W[N,K] (row-major, K contiguous).
+ *   w_dtype: 0 = fp16 bits (uint16), 1 = fp32
+ *   qweight: uint8 [N, K/2], element 2j in the low nibble, 2j+1 in the high nibble
+ *   scales : fp16 bits [N, K/128] (the fp32 scale rounded to nearest-even fp16)
+ *   zeros  : uint8 [N, K/128]
+ *   scales32 (optional, may be NULL): the fp32 scales, for tests of the bound.
+ * Returns 0, or -1 on invalid arguments. */
+int oracle_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K,
+                         uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
+                         float *scales32)
+{
+    if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    if (w_dtype != 0 && w_dtype != 1) return -1;
+    const int64_t ng = K / ORACLE_GROUP;
+    float wbuf[ORACLE_GROUP];
+    uint8_t qbuf[ORACLE_GROUP];
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < ng; ++g) {
+            const int64_t base = n * K + g * ORACLE_GROUP;
+            for (int i = 0; i < ORACLE_GROUP; ++i) {
+                if (w_dtype == 0)
+                    wbuf[i] = oracle_f16_to_f32(((const uint16_t *)W)[base + i]);
+                else
+                    wbuf[i] = ((const float *)W)[base + i];
+            }
+            float s;
+            int zp;
+            quantize_group(wbuf, ORACLE_GROUP, qbuf, &s, &zp);
+            scales[n * ng + g] = oracle_f32_to_f16_bits(s);
+            zeros[n * ng + g] = (uint8_t)zp;
+            if (scales32) scales32[n * ng + g] = s;
+            for (int j = 0; j < ORACLE_GROUP / 2; ++j) {
+                uint8_t lo = qbuf[2 * j], hi = qbuf[2 * j + 1];
+                qweight[n * (K / 2) + g * (ORACLE_GROUP / 2) + j] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return 0;
+}
+
+/* Unpack qweight[N,K/2] into q[N,K] (one value 0..15 per byte). */
+int oracle_unpack(const uint8_t *qweight, int64_t N, int64_t K, uint8_t *q)
+{
+    if (N < 0 || K < 0 || K % 2 != 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < K / 2; ++j) {
+            uint8_t b = qweight[n * (K / 2) + j];
+            q[n * K + 2 * j] = b & 0x0f;
+            q[n * K + 2 * j + 1] = (b >> 4) & 0x0f;
+        }
+    return 0;
+}
+
+/* Dequantize rows [n0, n0+rows) into out[rows, K] in fp64:
+ * w_hat[n,k] = (q[n,k] - zp[n,k/128]) * fp16_scale[n,k/128]  (exact in fp64). */
+static void dequant_rows(const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                         int64_t n0, int64_t rows, int64_t K, double *out)
+{
+    const int64_t ng = K / ORACLE_GROUP;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t n = n0 + r;
+        for (int64_t k = 0; k < K; ++k) {
+            uint8_t b = qweight[n * (K / 2) + k / 2];
+            int q = (k & 1) ? (b >> 4) & 0x0f : b & 0x0f;
+            int64_t g = k / ORACLE_GROUP;
+            double s = (double)oracle_f16_to_f32(scales[n * ng + g]);
+            int zp = zeros[n * ng + g];
+            out[r * K + k] = (double)(q - zp) * s;
+        }
+    }
+}
+
+int oracle_dequantize(const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                      int64_t N, int64_t K, double *W_hat)
+{
+    if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    dequant_rows(qweight, scales, zeros, 0, N, K, W_hat);
+    return 0;
+}
+
+/* W4A16 matmul in fp64:  Y[m,n] = sum_k A[m,k] * w_hat[n,k]   (A bf16 [M,K])
+ * and S[m,n] = sum_k |A[m,k] * w_hat[n,k]| (the scale of the tolerance).
+ * Follows the chunked dequantize-matmul pattern: dequantize a chunk of output rows,
+ * then take the dot products against every activation row. */
+int oracle_matmul(const uint16_t *A, int64_t M, int64_t N, int64_t K,
+                  const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                  double *Y, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    const int64_t chunk = 256;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    double *wc = (double *)malloc(sizeof(double) * (size_t)(chunk * K > 0 ? chunk * K : 1));
+    if (!a || !wc) { free(a); free(wc); return -2; }
+    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_bf16_to_f64(A[i]);
+    for (int64_t n0 = 0; n0 < N; n0 += chunk) {
+        int64_t rows = (N - n0 < chunk) ? N - n0 : chunk;
+        dequant_rows(qweight, scales, zeros, n0, rows, K, wc);
+        for (int64_t m = 0; m < M; ++m) {
+            for (int64_t r = 0; r < rows; ++r) {
+                double acc = 0.0, sab = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double p = a[m * K + k] * wc[r * K + k];
+                    acc += p;
+                    sab += fabs(p);
+                }
+                Y[m * N + n0 + r] = acc;
+                if (S) S[m * N + n0 + r] = sab;
+            }
+        }
+    }
+    free(a);
+    free(wc);
+    return 0;
+}
+
+/* The same quantity for a list of (m, n) output positions, one by one; used to
+ * check full-size outputs on a sample. */
+int oracle_matmul_entries(const uint16_t *A, int64_t M, int64_t N, int64_t K,
+                          const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                          const int64_t *mi, const int64_t *ni, int64_t count,
+                          double *Y, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    if (!w) return -2;
+    for (int64_t t = 0; t < count; ++t) {
+        int64_t m = mi[t], n = ni[t];
+        if (m < 0 || m >= M || n < 0 || n >= N) { free(w); return -1; }
+        dequant_rows(qweight, scales, zeros, n, 1, K, w);
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = oracle_bf16_to_f64(A[m * K + k]) * w[k];
+            acc += p;
+            sab += fabs(p);
+        }
+        Y[t] = acc;
+        if (S) S[t] = sab;
+    }
+    free(w);
+    return 0;
+}

@@ -1,0 +1,280 @@
+"""Pins for the CPU oracle: each test checks the oracle against something other
+than itself -- hand-worked groups, the page's printed packing vector, closed
+forms, exhaustive or exact-rational brute force, and library routines on special
+cases that reduce to them.  No expected value here comes from the CUDA path."""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import GOLDEN_DIR, parse_cases
+
+CASES = parse_cases(os.path.join(GOLDEN_DIR, "hand_groups.txt"))
+
+
+def _f32(bits):
+    return np.array([int(bits, 16)], dtype=np.uint32).view(np.float32)[0]
+
+
+def _group_from_case(case):
+    vals = [_f32(b) for b in case["values"].split()]
+    pad = _f32(case["pad"])
+    g = np.full(128, pad, dtype=np.float32)
+    g[: len(vals)] = vals
+    return g, len(vals)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c["name"] for c in CASES])
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_hand_worked_groups(oracle_mod, case, dtype):
+    g, nv = _group_from_case(case)
+    if dtype == "f16":
+        if case["f16_exact"] != "1":
+            pytest.skip("values not exact in fp16")
+        assert np.array_equal(g.astype(np.float16).astype(np.float32), g)
+        W = g.astype(np.float16)[None, :]
+    else:
+        W = g[None, :]
+    # Put the hand-worked group second in a row of three groups, so that the
+    # row/group indexing is exercised too; the other groups are plain N(0,1).
+    rng = np.random.default_rng(7)
+    row = rng.standard_normal(384).astype(W.dtype)
+    row[128:256] = W[0]
+    q, s16, z, s32 = oracle_mod.quantize_pack(row[None, :], with_fp32_scales=True)
+    assert s32[0, 1].view(np.uint32) == int(case["scale_f32"], 16)
+    assert s16[0, 1].view(np.uint16) == int(case["scale_f16"], 16)
+    assert z[0, 1] == int(case["zero"])
+    qq = oracle_mod.unpack(q, 384)[0, 128:256]
+    exp_q = [int(x) for x in case["q"].split()]
+    assert list(qq[:nv]) == exp_q
+    assert np.all(qq[nv:] == int(case["q_pad"]))
+    if "packed_prefix" in case:
+        pref = [int(x, 16) for x in case["packed_prefix"].split()]
+        packed = q[0, 64:128]
+        assert list(packed[: len(pref)]) == pref
+        assert np.all(packed[len(pref):] == int(case["packed_pad"], 16))
+
+
+def test_pack_unpack_identity(oracle_mod):
+    """Packing then unpacking returns the nibbles (the unpacker-integrity check of
+    the pure-Python GPTQ page, 'Running and Testing It')."""
+    rng = np.random.default_rng(11)
+    W = (rng.standard_normal((37, 512)) * 0.3).astype(np.float32)
+    q, s, z = oracle_mod.quantize_pack(W)
+    nib = oracle_mod.unpack(q, 512)
+    # Re-pack by the documented layout and compare bytes.
+    repacked = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(repacked, q)
+    assert nib.max() <= 15
+
+
+def test_ranges_and_endpoints(oracle_mod):
+    """zp and q in [0,15]; in an in-range group (min <= 0 <= max) the minimum maps
+    to level 0 and the maximum to level 15, unless the zero-point tie pushed the top
+    by exactly one level (then the max sits at 16 - 1 = 15 after the clip anyway)."""
+    rng = np.random.default_rng(3)
+    W = (rng.standard_normal((64, 1024)) * 0.05).astype(np.float16)
+    q, s16, z, s32 = oracle_mod.quantize_pack(W, with_fp32_scales=True)
+    nib = oracle_mod.unpack(q, 1024).reshape(64, 8, 128)
+    Wg = W.astype(np.float32).reshape(64, 8, 128)
+    assert z.max() <= 15 and nib.max() <= 15
+    for n in range(64):
+        for g in range(8):
+            w = Wg[n, g]
+            if w.min() <= 0 <= w.max() and w.min() < w.max():
+                assert nib[n, g][np.argmin(w)] <= 1
+                assert nib[n, g][np.argmax(w)] >= 14
+
+
+def test_reconstruction_bound(oracle_mod):
+    """|w - (q - zp) * s| <= s/2 (1 + 2^-20) for in-range groups, with the fp32 scale,
+    and |w - (q - zp) * s16| <= s/2 (1 + 2^-20) + 15 |s - s16| with the stored one."""
+    rng = np.random.default_rng(5)
+    for dtype, sigma in ((np.float16, 0.02), (np.float32, 1.0)):
+        W = (rng.standard_normal((96, 512)) * sigma).astype(dtype)
+        q, s16, z, s32 = oracle_mod.quantize_pack(W, with_fp32_scales=True)
+        nib = oracle_mod.unpack(q, 512).reshape(96, 4, 128).astype(np.float64)
+        w = W.astype(np.float64).reshape(96, 4, 128)
+        s = s32.astype(np.float64)[..., None]
+        s_st = s16.astype(np.float64)[..., None]
+        zz = z.astype(np.float64)[..., None]
+        inr = (w.min(-1) <= 0) & (w.max(-1) >= 0)
+        err = np.abs(w - (nib - zz) * s)
+        bound = s / 2 * (1 + 2.0 ** -20)
+        assert np.all(err[inr] <= np.broadcast_to(bound, err.shape)[inr])
+        err16 = np.abs(w - (nib - zz) * s_st)
+        b16 = bound + 15 * np.abs(s - s_st)
+        assert np.all(err16[inr] <= np.broadcast_to(b16, err.shape)[inr])
+
+
+def test_exact_rational_brute_force(oracle_mod):
+    """For each element, with the exact rational quotient x = w/s (Fraction), the
+    level q must be the integer in [0,15] nearest to x + zp (ties to even), except
+    when x lies within 2^-20 |x| of a half-integer, where fp32 rounding of the
+    quotient may legitimately decide.  zp is checked the same way from -min/s."""
+    rng = np.random.default_rng(17)
+    W = (rng.standard_normal((8, 256)) * 0.7).astype(np.float32)
+    W[3, :128] += 3.0           # an all-positive group (zp clipped to 0)
+    W[5, 128:] -= 4.0           # an all-negative group (zp clipped to 15)
+    q, s16, z, s32 = oracle_mod.quantize_pack(W, with_fp32_scales=True)
+    nib = oracle_mod.unpack(q, 256)
+
+    def near_half(x):
+        fl = math.floor(x)
+        return abs(x - fl - Fraction(1, 2)) <= abs(x) * Fraction(1, 2 ** 20)
+
+    checked = 0
+    for n in range(8):
+        for g in range(2):
+            w = W[n, 128 * g:128 * g + 128]
+            s = Fraction(float(s32[n, g]))
+            mn = Fraction(float(w.min()))
+            zx = -mn / s
+            if not near_half(zx):
+                # brute force over every level: the nearest one to the exact quotient
+                cand = min(range(-64, 80), key=lambda j: (abs(zx - j), j % 2))
+                assert z[n, g] == min(max(cand, 0), 15)
+            for i in range(128):
+                x = Fraction(float(w[i])) / s
+                if near_half(x):
+                    continue
+                # brute force: the nearest of all integers in a window around x
+                c = math.floor(x)
+                r = min(range(c - 2, c + 3), key=lambda j: (abs(x - j), j % 2))
+                expect = min(max(r + int(z[n, g]), 0), 15)
+                assert nib[n, 128 * g + i] == expect
+                checked += 1
+    assert checked > 1900
+
+
+def test_unit_scale_reduces_to_builtin_round(oracle_mod):
+    """Groups with min 0 and max 15 have s = 1 and zp = 0, so q = round(w) with
+    ties to even -- exactly Python's built-in round().  Run over every fp16 value
+    in [0, 15] (exhaustive)."""
+    allv = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float32)
+    vals = allv[(allv >= 0) & (allv <= 15)]
+    per = 126
+    ng = (len(vals) + per - 1) // per
+    W = np.zeros((ng, 128), np.float32)
+    W[:, 1] = 15.0
+    body = np.zeros(ng * per, np.float32)
+    body[: len(vals)] = vals
+    W[:, 2:] = body.reshape(ng, per)
+    q, s16, z, s32 = oracle_mod.quantize_pack(W, with_fp32_scales=True)
+    assert np.all(s32 == 1.0) and np.all(z == 0)
+    nib = oracle_mod.unpack(q, 128)[:, 2:].reshape(-1)[: len(vals)]
+    expect = np.array([round(float(v)) for v in vals])
+    assert np.array_equal(nib, expect)
+
+
+def test_constant_groups(oracle_mod):
+    """Constant groups take scale 1: zp = clip(round(-c)), q = clip(round(c) + zp)."""
+    cs = np.array([0.0, -0.0, 0.3, -0.3, 0.5, -0.5, 1.5, -2.6, 7.0, -20.0, 20.0], np.float32)
+    W = np.repeat(cs, 128).reshape(len(cs), 128)
+    q, s16, z, s32 = oracle_mod.quantize_pack(W, with_fp32_scales=True)
+    nib = oracle_mod.unpack(q, 128)
+    assert np.all(s32 == 1.0)
+    assert np.all(s16.view(np.uint16) == 0x3C00)
+    for i, c in enumerate(cs):
+        zr = min(max(round(-float(c)), 0), 15)
+        assert z[i, 0] == zr
+        assert np.all(nib[i] == min(max(round(float(c)) + zr, 0), 15))
+
+
+def test_f16_conversions_against_numpy(oracle_mod):
+    """The oracle's own binary16 codecs agree with numpy's (a library routine):
+    widening exhaustively over all finite patterns, narrowing on a spread of fp32
+    values including ties, subnormals and overflow."""
+    for bits in list(range(0, 0x7C00, 37)) + [0x0001, 0x03FF, 0x0400, 0x7BFF, 0x8001, 0xFBFF]:
+        ref = float(np.array([bits], np.uint16).view(np.float16)[0])
+        assert oracle_mod.f16_to_f32(bits) == ref
+    rng = np.random.default_rng(1)
+    xs = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * 10,
+        (rng.standard_normal(500) * 1e-6).astype(np.float32),    # subnormal range
+        np.array([65504, 65519, 65520, 70000, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                  1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 0.1, 1 / 15], np.float32),
+    ])
+    for x in xs:
+        with np.errstate(over="ignore"):
+            ref = int(np.array([x], np.float32).astype(np.float16).view(np.uint16)[0])
+        assert oracle_mod.f32_to_f16_bits(float(x)) == ref, x
+
+
+def test_matmul_integer_special_case(oracle_mod):
+    """With s = 1 and zp = 0 (groups spanning exactly [0, 15] in integers) the
+    dequantized weights are the integers q; with small-integer activations the fp64
+    result is exact and equals numpy's int64 matmul (a library routine)."""
+    rng = np.random.default_rng(23)
+    N, K, M = 9, 384, 5
+    Wi = rng.integers(0, 16, size=(N, K))
+    Wi[:, 0::128] = 0
+    Wi[:, 1::128] = 15
+    q, s16, z = oracle_mod.quantize_pack(Wi.astype(np.float32))
+    assert np.all(s16 == 1.0) and np.all(z == 0)
+    Ai = rng.integers(-8, 9, size=(M, K))
+    A_bits = (Ai.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16
+    Y, S = oracle_mod.matmul(A_bits, q, s16, z)
+    assert np.array_equal(Y, (Ai @ Wi.T).astype(np.float64))
+    assert np.array_equal(S, (np.abs(Ai) @ np.abs(Wi).T).astype(np.float64))
+
+
+def test_fused_matmul_equals_explicit_dequant(oracle_mod):
+    """The chunked fused matmul equals dequantize-then-matmul (numpy fp64 matmul,
+    a library routine) on tiny non-square shapes, relative 1e-12.  The shapes use
+    more than one chunk of 256 output rows."""
+    rng = np.random.default_rng(29)
+    N, K, M = 300, 256, 3
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    q, s16, z = oracle_mod.quantize_pack(W)
+    A = (rng.standard_normal((M, K)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    Y, S = oracle_mod.matmul(A, q, s16, z)
+    Wd = oracle_mod.dequantize(q, s16, z, K)
+    Af = (A.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Yd = Af @ Wd.T
+    assert np.allclose(Y, Yd, rtol=1e-12, atol=1e-15)
+    assert np.all(S >= np.abs(Y) * (1 - 1e-12))
+    assert np.allclose(S, np.abs(Af) @ np.abs(Wd).T, rtol=1e-12)
+    # sampled entries agree with the full result
+    mi = np.array([0, 2, 1, 2]); ni = np.array([0, 299, 256, 17])
+    Ye, Se = oracle_mod.matmul_entries(A, q, s16, z, mi, ni)
+    assert np.array_equal(Ye, Y[mi, ni]) and np.array_equal(Se, S[mi, ni])
+
+
+def test_dequant_hand_values(oracle_mod):
+    """Reconstruction of the hand-worked groups: H1 (s16 = 1, zp = 8) gives q - 8;
+    H4b gives -3 everywhere; H2 gives (q - 8) * 0.0999755859375."""
+    by = {c["name"]: c for c in CASES}
+    g1, _ = _group_from_case(by["H1"])
+    g4, _ = _group_from_case(by["H4b"])
+    g2, _ = _group_from_case(by["H2"])
+    W = np.stack([g1, g4, g2])
+    q, s16, z = oracle_mod.quantize_pack(W)
+    d = oracle_mod.dequantize(q, s16, z, 128)
+    assert list(d[0, :6]) == [-8.0, 0.0, 0.0, 2.0, 2.0, 7.0]
+    assert np.all(d[1] == -3.0)
+    assert list(d[2, :3]) == [-8 * 0.0999755859375, 7 * 0.0999755859375, 0.0]
+
+
+def test_tolerance_closed_forms(oracle_mod):
+    """ulp of bf16 (8 significant bits): 2^(e-7) in the binade [2^e, 2^(e+1)),
+    2^-133 at zero and in the subnormal range."""
+    u = oracle_mod.ulp_bf16(np.array([1.0, 1.5, 1.99, 2.0, 3.0, 0.0, 2.0 ** -130, -4.0]))
+    assert list(u) == [2.0 ** -7, 2.0 ** -7, 2.0 ** -7, 2.0 ** -6, 2.0 ** -6,
+                       2.0 ** -133, 2.0 ** -133, 2.0 ** -5]
+    Yref = np.array([1.0, -3.0, 0.0])
+    S = np.array([2.0, 3.0, 0.0])
+    bits = np.array([0x3F80, 0xC040, 0x0000], np.uint16)   # 1.0, -3.0, 0.0 exactly
+    ok, worst, _ = oracle_mod.check_y(bits, Yref, S)
+    assert ok and worst == 0.0
+    # one bf16 step off on 1.0 (1.0078125): error 2^-7 > 8e-3*2 + 2^-8? 0.0078 < 0.0199 -> ok
+    ok, _, _ = oracle_mod.check_y(np.array([0x3F81, 0xC040, 0x0000], np.uint16), Yref, S)
+    assert ok
+    # error above the bound fails
+    ok, _, _ = oracle_mod.check_y(np.array([0x3F90, 0xC040, 0x0000], np.uint16), Yref, S)
+    assert not ok
+    # a nonzero output where the reference is exactly 0 with S = 0 fails
+    ok, _, _ = oracle_mod.check_y(np.array([0x3F80, 0xC040, 0x0001], np.uint16), Yref, S)
+    assert not ok
