@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every function include/w4a16.h declares, and rejects invalid arguments
+with the documented status before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_matmul_asym_b300 import build
+    build.build()
+    import w4a16_matmul_asym_b300 as w4
+    return w4.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("w4_quantize_pack", "w4_matmul", "w4_status_string", "w4_check_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    import w4a16_matmul_asym_b300 as w4
+    assert set(w4.EXPORTED) == set(declared_functions())
+
+
+def test_status_strings(lib):
+    import w4a16_matmul_asym_b300 as w4
+    for code in range(6):
+        s = w4.status_string(code)
+        assert s and s.startswith("W4_")
+    assert "unknown" in w4.status_string(99)
+
+
+FAKE = 0x10000  # a 16-byte-aligned, never-dereferenced address
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, 0, -1, 128, 128), 1),        # negative N
+    ((FAKE, 0, 4, -128, 128), 1),        # negative K
+    ((FAKE, 0, 4, 130, 128), 1),         # K not a multiple of the group (checked after group)
+    ((FAKE, 0, 4, 128, 64), 2),          # group 64 unsupported
+    ((FAKE, 0, 4, 128, 0), 1),           # group 0
+    ((FAKE, 7, 4, 128, 128), 1),         # unknown dtype
+    ((0, 0, 4, 128, 128), 1),            # null W
+    ((FAKE + 8, 0, 4, 128, 128), 3),     # misaligned W
+    ((FAKE, 0, 0, 128, 128), 0),         # empty: N == 0
+    ((FAKE, 0, 4, 0, 128), 0),           # empty: K == 0
+])
+def test_quantize_pack_validation(lib, args, expect):
+    W, dt, N, K, G = args
+    rc = lib.w4_quantize_pack(W, dt, N, K, G, FAKE, FAKE, FAKE, None)
+    assert rc == expect
+
+
+def test_quantize_pack_null_and_misaligned_outputs(lib):
+    assert lib.w4_quantize_pack(FAKE, 0, 4, 128, 128, 0, FAKE, FAKE, None) == 1
+    assert lib.w4_quantize_pack(FAKE, 0, 4, 128, 128, FAKE, 0, FAKE, None) == 1
+    assert lib.w4_quantize_pack(FAKE, 0, 4, 128, 128, FAKE, FAKE, 0, None) == 1
+    assert lib.w4_quantize_pack(FAKE, 0, 4, 128, 128, FAKE + 4, FAKE, FAKE, None) == 3
+    assert lib.w4_quantize_pack(FAKE, 0, 4, 128, 128, FAKE, FAKE + 1, FAKE, None) == 3
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, -1, 4, 128, 128), 1),
+    ((FAKE, 1, -4, 128, 128), 1),
+    ((FAKE, 1, 4, -128, 128), 1),
+    ((FAKE, 1, 4, 100, 128), 1),
+    ((FAKE, 1, 4, 256, 32), 2),
+    ((FAKE, 0, 4, 256, 128), 0),         # M == 0: nothing to do
+    ((FAKE, 3, 0, 256, 128), 0),         # N == 0: nothing to do
+    ((0, 3, 4, 256, 128), 1),            # null A
+    ((FAKE + 2, 3, 4, 256, 128), 3),     # misaligned A
+])
+def test_matmul_validation(lib, args, expect):
+    A, M, N, K, G = args
+    rc = lib.w4_matmul(A, M, N, K, G, FAKE, FAKE, FAKE, FAKE, None)
+    assert rc == expect
+
+
+def test_matmul_null_and_misaligned(lib):
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, 0, FAKE, FAKE, FAKE, None) == 1
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE, 0, FAKE, FAKE, None) == 1
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE, FAKE, 0, FAKE, None) == 1
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE, FAKE, FAKE, 0, None) == 1
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE + 8, FAKE, FAKE, FAKE, None) == 3
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE, FAKE + 1, FAKE, FAKE, None) == 3
+    assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE, FAKE, FAKE, FAKE + 1, None) == 3
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from w4a16_matmul_asym_b300 import _binding
+    with pytest.raises(ImportError):
+        _binding._lib_saved = _binding._lib
+        try:
+            _binding._lib = None
+            _binding.load_library(str(tmp_path / "missing.so"))
+        finally:
+            _binding._lib = _binding._lib_saved

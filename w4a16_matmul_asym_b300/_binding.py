@@ -1,0 +1,151 @@
+"""ctypes binding of libw4a16.so: the C entry points under the same names, plus
+torch-tensor conveniences that allocate outputs and pass the current stream.
+
+Argument marshalling only: every step of quantization and of the matmul runs in
+the library's CUDA kernels.  There is no CPU path; if the library is missing the
+import fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libw4a16.so")
+
+W4_OK = 0
+W4_ERR_INVALID_ARG = 1
+W4_ERR_UNSUPPORTED = 2
+W4_ERR_MISALIGNED = 3
+W4_ERR_CUDA = 4
+W4_ERR_TIMEOUT = 5
+W4_DTYPE_F16 = 0
+W4_DTYPE_F32 = 1
+GROUP_SIZE = 128
+
+# Symbols declared in include/w4a16.h (checked by the host-side tests).
+EXPORTED = ("w4_quantize_pack", "w4_matmul", "w4_status_string", "w4_check_device_error",
+            "w4_set_wait_timeout_ns", "w4_debug_inject_stall")
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libw4a16.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m w4a16_matmul_asym_b300.build` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.w4_quantize_pack.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+    lib.w4_quantize_pack.restype = ctypes.c_int
+    lib.w4_matmul.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp]
+    lib.w4_matmul.restype = ctypes.c_int
+    lib.w4_status_string.argtypes = [ctypes.c_int]
+    lib.w4_status_string.restype = ctypes.c_char_p
+    lib.w4_check_device_error.argtypes = [vp]
+    lib.w4_check_device_error.restype = ctypes.c_int
+    lib.w4_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.w4_set_wait_timeout_ns.restype = None
+    lib.w4_debug_inject_stall.argtypes = [ctypes.c_int]
+    lib.w4_debug_inject_stall.restype = None
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().w4_status_string(int(status)).decode()
+
+
+# ---- raw C entry points (pointers and sizes) -------------------------------------
+def w4_quantize_pack(W_ptr: int, w_dtype: int, N: int, K: int, group: int,
+                     qweight_ptr: int, scales_ptr: int, zeros_ptr: int, stream: int) -> int:
+    return load_library().w4_quantize_pack(W_ptr, w_dtype, N, K, group, qweight_ptr,
+                                           scales_ptr, zeros_ptr, stream)
+
+
+def w4_matmul(A_ptr: int, M: int, N: int, K: int, group: int, qweight_ptr: int,
+              scales_ptr: int, zeros_ptr: int, Y_ptr: int, stream: int) -> int:
+    return load_library().w4_matmul(A_ptr, M, N, K, group, qweight_ptr, scales_ptr,
+                                    zeros_ptr, Y_ptr, stream)
+
+
+def w4_check_device_error(stream: int = 0) -> int:
+    return load_library().w4_check_device_error(stream)
+
+
+def w4_set_wait_timeout_ns(ns: int) -> None:
+    load_library().w4_set_wait_timeout_ns(int(ns))
+
+
+def w4_debug_inject_stall(enable: bool) -> None:
+    load_library().w4_debug_inject_stall(1 if enable else 0)
+
+
+# ---- torch conveniences ------------------------------------------------------------
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def quantize_pack(W, group: int = GROUP_SIZE, stream=None, out=None):
+    """Quantize a CUDA tensor W[N,K] (float16 or float32).
+
+    Returns (qweight uint8 [N,K/2], scales float16 [N,K/128], zeros uint8 [N,K/128]),
+    allocated with torch on W's device unless `out` supplies them.
+    """
+    import torch
+    if W.dim() != 2 or not W.is_cuda:
+        raise ValueError("W must be a 2-D CUDA tensor")
+    if W.dtype == torch.float16:
+        dt = W4_DTYPE_F16
+    elif W.dtype == torch.float32:
+        dt = W4_DTYPE_F32
+    else:
+        raise TypeError("W must be float16 or float32")
+    W = W.contiguous()
+    N, K = W.shape
+    if out is None:
+        ng = K // group if group > 0 else 0
+        qweight = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+        scales = torch.empty((N, ng), dtype=torch.float16, device=W.device)
+        zeros = torch.empty((N, ng), dtype=torch.uint8, device=W.device)
+    else:
+        qweight, scales, zeros = out
+    rc = w4_quantize_pack(W.data_ptr(), dt, N, K, group, qweight.data_ptr(),
+                          scales.data_ptr(), zeros.data_ptr(), _stream_handle(stream))
+    if rc != W4_OK:
+        raise W4Error(rc, "w4_quantize_pack")
+    return qweight, scales, zeros
+
+
+def matmul(A, qweight, scales, zeros, group: int = GROUP_SIZE, stream=None, out=None):
+    """Y[M,N] = A[M,K] (bfloat16, CUDA) times the dequantized weights, as bfloat16."""
+    import torch
+    if A.dim() != 2 or not A.is_cuda or A.dtype != torch.bfloat16:
+        raise ValueError("A must be a 2-D bfloat16 CUDA tensor")
+    A = A.contiguous()
+    M, K = A.shape
+    N = qweight.shape[0]
+    if qweight.dtype != torch.uint8 or zeros.dtype != torch.uint8 or scales.dtype != torch.float16:
+        raise TypeError("qweight/zeros must be uint8 and scales float16")
+    if tuple(qweight.shape) != (N, K // 2):
+        raise ValueError(f"qweight shape {tuple(qweight.shape)} does not match K={K}")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    rc = w4_matmul(A.data_ptr(), M, N, K, group, qweight.data_ptr(), scales.data_ptr(),
+                   zeros.data_ptr(), Y.data_ptr(), _stream_handle(stream))
+    if rc != W4_OK:
+        raise W4Error(rc, "w4_matmul")
+    return Y

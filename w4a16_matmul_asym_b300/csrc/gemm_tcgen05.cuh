@@ -1,0 +1,545 @@
+// gemm_tcgen05.cuh -- prefill-shaped W4A16 GEMM (M >= 9) on the 5th-generation
+// tensor cores: Y[M,N] = A[M,K] * W_hat[N,K]^T, W_hat = (q - zp) * s16.
+//
+// The contraction is the fused dequantize-matmul of "Build a GPTQ INT4 Quantization
+// Engine in Python/NumPy" (Step 5) with the dequantization of "From Scratch: Building a
+// GPTQ INT4 Quantizer in Pure Python" (Step 4); "Building a From-Scratch Group-Wise INT4
+// Quantization Layer for LLaMA Weights" (Architecture Overview) names fused
+// dequant + matmul as the hot path.  The full-precision W never exists in global memory:
+// each 256 x 64 tile of packed W is dequantized to bf16 in shared memory and consumed
+// there by tcgen05.mma.
+//
+// One persistent CTA per SM (512 threads), tiles of 128 (M) x 256 (N), k-blocks of 64:
+//   warp 0      TMA producer: A tile (bf16, 128B-swizzled) + packed W tile (256 x 32 B)
+//   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma (M128 N256 K16,
+//               bf16 x bf16 -> fp32) into one of two accumulators, commits to mbarriers
+//   warps 4-7   epilogue: tcgen05.ld 32 columns at a time -> bf16 -> global stores
+//   warps 8-15  dequantize: thread r owns tile row r, turns its 32 packed bytes into
+//               64 bf16 written in the 128B-swizzled K-major layout the MMA reads
+// Pipelines: 4 stages of (A, packed W), 3 stages of dequantized W, 2 accumulators, so
+// copies, dequantization, MMAs and the epilogue of the previous tile overlap.
+// Every wait is bounded (see common.cuh); on a timeout the CTA drains its copies and
+// MMAs, frees TMEM and exits, leaving W4_ERR_TIMEOUT in the device error word.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace w4 {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int SA = 4;                         // (A, packed W) stages
+constexpr int SD = 3;                         // dequantized-W stages
+constexpr int A_STAGE = BM * BK * 2;          // 16 KB
+constexpr int BQ_STAGE = BN * BK / 2;         // 8 KB
+constexpr int BD_STAGE = BN * BK * 2;         // 32 KB
+constexpr int NUM_THREADS = 512;
+constexpr int EPI_WARP0 = 4;
+constexpr int DEQ_WARP0 = 8;
+constexpr int NUM_DEQ_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;           // two BN-column fp32 accumulators
+
+constexpr int OFF_A = 0;
+constexpr int OFF_BD = OFF_A + SA * A_STAGE;
+constexpr int OFF_BQ = OFF_BD + SD * BD_STAGE;
+constexpr int OFF_BAR = OFF_BQ + SA * BQ_STAGE;
+constexpr int NUM_BARS = 2 * SA + 2 * SD + 4 + 2;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16;
+constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
+
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 D, bf16 A and B, both
+// K-major, N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait that ignores the abort flag (used while draining after an abort).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                unsigned long long timeout_ns) {
+    const uint32_t a = smem_addr(bar);
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            record_error(W4_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Lane 0 waits, the result is broadcast, so the warp leaves the wait converged.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned long long timeout_ns) {
+    int ok = 1;
+    if (lane_id() == 0) ok = mbar_wait(bar, parity, abort_flag, timeout_ns) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;  // (a & b) | c
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 8 packed levels (element 2j low nibble) -> 8 bf16 (q - zp) * s, in k order.
+// Each nibble pair is spread into the two halves of a word with prmt, masked and
+// ORed with the bf16 pattern of 128 (ulp 1), giving 128 + q exactly; subtracting
+// 128 + zp is exact; the multiply by the bf16 scale rounds once.
+__device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t zz2, uint32_t s2) {
+    const uint32_t x4 = x >> 4;
+    const uint32_t magic = 0x43004300u, mask = 0x000F000Fu;
+    uint4 o;
+    o.x = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0400u), mask, magic), zz2), s2);
+    o.y = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0501u), mask, magic), zz2), s2);
+    o.z = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0602u), mask, magic), zz2), s2);
+    o.w = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0703u), mask, magic), zz2), s2);
+    return o;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float f) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+struct Params {
+    const __half *scales;
+    const uint8_t *zeros;
+    __nv_bfloat16 *Y;
+    int M, N, K;
+    int vec_store;  // Y rows are 16-byte aligned (N % 8 == 0 and Y 16-byte aligned)
+    WaitParams wait;
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    // Align the shared-window offset (not the generic address) to 1024 bytes, as the
+    // 128-byte swizzle pattern of TMA and of the MMA descriptors assumes.
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = smem + OFF_A;
+    uint8_t *sBd = smem + OFF_BD;
+    uint8_t *sBq = smem + OFF_BQ;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *full_ab = bars;
+    uint64_t *empty_ab = full_ab + SA;
+    uint64_t *full_d = empty_ab + SA;
+    uint64_t *empty_d = full_d + SD;
+    uint64_t *tmem_full = empty_d + SD;
+    uint64_t *tmem_empty = tmem_full + 2;
+    uint64_t *mma_done = tmem_empty + 2;
+    uint64_t *never = mma_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m_tiles = (p.M + BM - 1) / BM;
+    const int n_tiles = (p.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int KB = p.K / BK;
+    const unsigned long long tmo = p.wait.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(&full_ab[s], 1);
+            mbar_init(&empty_ab[s], 1 + NUM_DEQ_WARPS);
+        }
+        for (int s = 0; s < SD; ++s) {
+            mbar_init(&full_d[s], NUM_DEQ_WARPS);
+            mbar_init(&empty_d[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&tmem_full[s], 1);
+            mbar_init(&tmem_empty[s], 4);
+        }
+        mbar_init(mma_done, 1);
+        mbar_init(never, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            int issued_parity[SA];
+#pragma unroll
+            for (int s = 0; s < SA; ++s) issued_parity[s] = -1;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int mt = tile % m_tiles, nt = tile / m_tiles;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&empty_ab[stage], phase ^ 1u, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_ab[stage], A_STAGE + BQ_STAGE);
+                    tma_load_2d(sA + stage * A_STAGE, &tmA, &full_ab[stage], kb * BK, mt * BM, pol);
+                    tma_load_2d(sBq + stage * BQ_STAGE, &tmB, &full_ab[stage], kb * (BK / 2),
+                                nt * BN, pol);
+#pragma unroll
+                    for (int s = 0; s < SA; ++s)
+                        if (s == static_cast<int>(stage)) issued_parity[s] = static_cast<int>(phase);
+                    if (++stage == SA) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Drain: every copy this thread issued must land before the CTA exits.
+#pragma unroll
+                for (int s = 0; s < SA; ++s)
+                    if (issued_parity[s] >= 0)
+                        mbar_wait_drain(&full_ab[s], static_cast<uint32_t>(issued_parity[s]), tmo);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, dstage = 0, dphase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            if (p.wait.stall) ok = mbar_wait(never, 0, abort_flag, tmo);  // test hook
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, tmo)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&full_ab[stage], phase, abort_flag, tmo) ||
+                        !mbar_wait(&full_d[dstage], dphase, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_addr(sA + stage * A_STAGE);
+                    const uint32_t b_addr = smem_addr(sBd + dstage * BD_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                                  kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit(&empty_ab[stage]);
+                    umma_commit(&empty_d[dstage]);
+                    if (++stage == SA) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (++dstage == SD) {
+                        dstage = 0;
+                        dphase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tmem_full[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // All MMAs issued by this thread complete before TMEM is released.
+            umma_commit(mma_done);
+            mbar_wait_drain(mma_done, 0, tmo);
+        }
+        __syncwarp();
+    } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
+        // ---------------- epilogue: TMEM -> bf16 -> global ----------------
+        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int mt = tile % m_tiles, nt = tile / m_tiles;
+            if (!warp_wait(&tmem_full[acc], acc_phase, abort_flag, tmo)) break;
+            tc_fence_after();
+            const int gm = mt * BM + quarter * 32 + lane;
+            __nv_bfloat16 *yrow = p.Y + static_cast<int64_t>(gm) * p.N;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + c, v);
+                tmem_wait_ld();
+                const int gn = nt * BN + c;
+                if (gm < p.M && gn < p.N) {
+                    if (p.vec_store && gn + 32 <= p.N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + gn);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                                                pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (gn + j < p.N) yrow[gn + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    } else if (warp >= DEQ_WARP0) {
+        // ---------------- dequantize packed W -> swizzled bf16 ----------------
+        const int r = threadIdx.x - DEQ_WARP0 * 32;  // tile row owned by this thread
+        const int ng = p.K / 128;
+        uint32_t stage = 0, phase = 0, dstage = 0, dphase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const int nt = tile / m_tiles;
+            const int n = nt * BN + r;
+            const bool valid = n < p.N;
+            const int64_t sz_row = static_cast<int64_t>(n) * ng;
+            // Scales / zero points run two groups ahead of use.
+            uint32_t s_cur = 0, z_cur = 0, s_nx1 = 0, z_nx1 = 0, s_nx2 = 0, z_nx2 = 0;
+            if (valid) {
+                s_nx1 = __half_as_ushort(p.scales[sz_row]);
+                z_nx1 = p.zeros[sz_row];
+                if (ng > 1) {
+                    s_nx2 = __half_as_ushort(p.scales[sz_row + 1]);
+                    z_nx2 = p.zeros[sz_row + 1];
+                }
+            }
+            uint32_t s2 = 0, zz2 = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                if ((kb & 1) == 0) {
+                    const int g = kb >> 1;
+                    s_cur = s_nx1;
+                    z_cur = z_nx1;
+                    s_nx1 = s_nx2;
+                    z_nx1 = z_nx2;
+                    if (valid && g + 2 < ng) {
+                        s_nx2 = __half_as_ushort(p.scales[sz_row + g + 2]);
+                        z_nx2 = p.zeros[sz_row + g + 2];
+                    }
+                    // bf16(s16) twice, and 128 + zp (exact) twice; invalid rows give 0.
+                    const uint32_t sb = valid ? bf16_bits(__half2float(__ushort_as_half(
+                                                    static_cast<unsigned short>(s_cur))))
+                                              : 0u;
+                    const uint32_t zb = bf16_bits(128.0f + static_cast<float>(z_cur));
+                    s2 = sb | (sb << 16);
+                    zz2 = zb | (zb << 16);
+                }
+                if (!warp_wait(&full_ab[stage], phase, abort_flag, tmo)) {
+                    ok = false;
+                    break;
+                }
+                const uint4 *src = reinterpret_cast<const uint4 *>(sBq + stage * BQ_STAGE + r * 32);
+                const uint4 w0 = src[0], w1 = src[1];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_ab[stage]);
+                if (!warp_wait(&empty_d[dstage], dphase ^ 1u, abort_flag, tmo)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *row_base = sBd + dstage * BD_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
+                const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 o = dequant8(words[c], zz2, s2);
+                    *reinterpret_cast<uint4 *>(row_base + ((c ^ (r & 7)) << 4)) = o;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_d[dstage]);
+                if (++stage == SA) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++dstage == SD) {
+                    dstage = 0;
+                    dphase ^= 1u;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- host side ------------------------------------------------------------------
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+inline bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gemm
+
+inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K,
+                               const uint8_t *qweight, const __half *scales, const uint8_t *zeros,
+                               __nv_bfloat16 *Y, cudaStream_t stream, int sms, WaitParams wp) {
+    using namespace gemm;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return W4_ERR_UNSUPPORTED;
+    CUtensorMap tmA, tmB;
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_CUDA;
+    if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, K / 2, N, K / 2, BK / 2, BN,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4_ERR_CUDA;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4_ERR_CUDA;
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    if (dev < 0 || dev >= 64) return W4_ERR_CUDA;
+    std::call_once(attr_once[dev], [&]() {
+        attr_err[dev] = cudaFuncSetAttribute(w4a16_gemm_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    });
+    if (attr_err[dev] != cudaSuccess) return W4_ERR_CUDA;
+
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    Params prm;
+    prm.scales = scales;
+    prm.zeros = zeros;
+    prm.Y = Y;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(Y) & 15) == 0) ? 1 : 0;
+    prm.wait = wp;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = stream;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel, tmA, tmB, prm);
+    return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+}  // namespace w4
