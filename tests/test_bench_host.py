@@ -1,0 +1,72 @@
+"""Host-side logic of bench.py: byte/flop accounting and the multi-rank control plane
+(two gloo ranks on CPU: max-over-ranks time, sum-over-ranks units)."""
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def test_algorithmic_bytes_match_the_stated_figures():
+    # Llama-7B decode workload: W fp16 [11008, 4096], A [1, 4096]
+    assert bench.quantize_bytes(11008, 4096, 2) == 113_778_688
+    assert bench.matmul_bytes(1, 11008, 4096) == 23_631_360
+    # 70B MLP layer: W fp16 [28672, 8192]
+    assert bench.quantize_bytes(28672, 8192, 2) == 592_707_584
+    assert bench.matmul_bytes(1, 28672, 8192) == 123_019_264
+    # skinny M = 8 and prefill GEMM
+    assert bench.matmul_bytes(8, 4096, 4096) == 8_912_896
+    assert bench.matmul_flops(2048, 14336, 4096) == 240_518_168_576
+    # tiny fp32 case
+    assert bench.quantize_bytes(128, 256, 4) == 148_224
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench as b
+    d = b.dist_init(world)
+    t, u = b.aggregate(1.0 + rank, 10.0 * (rank + 1), d)
+    b.barrier(d)
+    q.put((rank, t, u))
+    d.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t, u in out:
+        assert t == 2.0          # max over ranks
+        assert u == 30.0         # sum over ranks
+
+
+def test_single_rank_aggregation_is_identity():
+    assert bench.aggregate(3.5, 7.0, None) == (3.5, 7.0)
+
+
+def test_reference_arm_runs_on_cpu(capsys):
+    """The reference arm (CPU oracle alone) prints one JSON line with impl=reference."""
+    import json
+    rc = bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3",
+                     "--workload", "tiny"])
+    assert rc == 0
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"

@@ -5,19 +5,27 @@
 // Engine in Python/NumPy" (Step 5) with the dequantization of "From Scratch: Building a
 // GPTQ INT4 Quantizer in Pure Python" (Step 4); "Building a From-Scratch Group-Wise INT4
 // Quantization Layer for LLaMA Weights" (Architecture Overview) names fused
-// dequant + matmul as the hot path.  The full-precision W never exists in global memory:
-// each 256 x 64 tile of packed W is dequantized to bf16 in shared memory and consumed
-// there by tcgen05.mma.
+// dequant + matmul as the hot path.  The full-precision W never exists in memory:
+// each 128 x 64 tile of packed W is dequantized to bf16 straight into tensor memory.
 //
-// One persistent CTA per SM (512 threads), tiles of 128 (M) x 256 (N), k-blocks of 64:
-//   warp 0      TMA producer: A tile (bf16, 128B-swizzled) + packed W tile (256 x 32 B)
-//   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma (M128 N256 K16,
-//               bf16 x bf16 -> fp32) into one of two accumulators, commits to mbarriers
-//   warps 4-7   epilogue: tcgen05.ld 32 columns at a time -> bf16 -> global stores
-//   warps 8-15  dequantize: thread r owns tile row r, turns its 32 packed bytes into
-//               64 bf16 written in the 128B-swizzled K-major layout the MMA reads
-// Pipelines: 4 stages of (A, packed W), 3 stages of dequantized W, 2 accumulators, so
-// copies, dequantization, MMAs and the epilogue of the previous tile overlap.
+// The kernel computes the transposed product Y^T = W_hat * A^T so that the
+// dequantized weights are the MMA's A operand, which tcgen05.mma reads from tensor
+// memory (TMEM): MMA M = 128 rows of W, MMA N = MT rows of A (16..256, multiple of
+// 16), K = 16 per instruction.  The activations are the B operand, loaded by TMA into
+// 128-byte-swizzled shared memory.  Dequantized weights never touch shared memory,
+// and every dequantized weight serves MT activation rows.
+//
+// One persistent CTA per SM, 640 threads (20 warps):
+//   warp 0        TMA producer: activation tile [MT x 64] bf16 + packed W [128 x 32 B]
+//   warp 1        allocates all 512 TMEM columns; one lane issues the MMAs
+//   warps 4-11    epilogue: two warps per TMEM lane quarter, each draining half of the
+//                 accumulator columns, 32 at a time, to bf16 Y (one warp store writes
+//                 32 consecutive n of one row of Y)
+//   warps 12-19   dequantize: two warps per lane quarter; thread = one row of the W
+//                 tile, 32 of its 64 k per k-block -> tcgen05.st into a TMEM A stage
+// TMEM: columns [0, 256) accumulators (two of 128 when MT <= 128, one of 256 otherwise),
+// columns [256, 512) eight A-operand stages of 32 columns (64 bf16 per lane).
+// Shared memory: 5 stages of (activation tile, packed W tile).
 // Every wait is bounded (see common.cuh); on a timeout the CTA drains its copies and
 // MMAs, frees TMEM and exits, leaving W4_ERR_TIMEOUT in the device error word.
 #pragma once
@@ -31,34 +39,36 @@
 namespace w4 {
 namespace gemm {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int SA = 4;                         // (A, packed W) stages
-constexpr int SD = 3;                         // dequantized-W stages
-constexpr int A_STAGE = BM * BK * 2;          // 16 KB
-constexpr int BQ_STAGE = BN * BK / 2;         // 8 KB
-constexpr int BD_STAGE = BN * BK * 2;         // 32 KB
-constexpr int NUM_THREADS = 512;
+constexpr int BW = 128;                       // W rows per tile (MMA M, TMEM lanes)
+constexpr int BK = 64;                        // k per stage
+constexpr int MT_MAX = 256;                   // activation rows per tile (MMA N), max
+constexpr int SA = 5;                         // (activation, packed W) smem stages
+constexpr int ST = 8;                         // TMEM A-operand stages
+constexpr int ACT_STAGE_MAX = MT_MAX * BK * 2;  // 32 KB
+constexpr int BQ_STAGE = BW * BK / 2;         // 4 KB
+constexpr int STAGE_BYTES = ACT_STAGE_MAX + BQ_STAGE;
+constexpr int NUM_THREADS = 640;
 constexpr int EPI_WARP0 = 4;
-constexpr int DEQ_WARP0 = 8;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int DEQ_WARP0 = 12;
 constexpr int NUM_DEQ_WARPS = 8;
-constexpr uint32_t TMEM_COLS = 512;           // two BN-column fp32 accumulators
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = 256;            // accumulator region
+constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
 
-constexpr int OFF_A = 0;
-constexpr int OFF_BD = OFF_A + SA * A_STAGE;
-constexpr int OFF_BQ = OFF_BD + SD * BD_STAGE;
-constexpr int OFF_BAR = OFF_BQ + SA * BQ_STAGE;
-constexpr int NUM_BARS = 2 * SA + 2 * SD + 4 + 2;
+constexpr int OFF_STAGES = 0;
+constexpr int OFF_BAR = OFF_STAGES + SA * STAGE_BYTES;
+constexpr int NUM_BARS = 2 * SA + 2 * ST + 4 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 D, bf16 A and B, both
-// K-major, N = BN, M = BM.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+// K-major, N = mt, M = 128.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t mt) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((mt >> 3) << 17) |
+           (static_cast<uint32_t>(BW >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -91,27 +101,37 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
             smem_addr(bar))
         : "memory");
 }
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
+__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+// 16 consecutive 32-bit columns of this thread's TMEM lane <- registers.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 8 consecutive 32-bit columns of this thread's TMEM lane -> registers.
+__device__ __forceinline__ void tmem_ld_8cols(uint32_t taddr, uint32_t *v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-          "=r"(v[31])
-        : "r"(taddr));
+          "=r"(v[7])
+        : "r"(taddr)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -137,7 +157,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     int ok = 1;
     if (lane_id() == 0) ok = mbar_wait(bar, parity, abort_flag, timeout_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
+    __syncwarp();  // orders the other lanes' accesses after lane 0's acquire
     return ok != 0;
 }
 
@@ -162,28 +182,21 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return d;
 }
 
-// 8 packed levels (element 2j low nibble) -> 8 bf16 (q - zp) * s, in k order.
-// Each nibble pair is spread into the two halves of a word with prmt, masked and
-// ORed with the bf16 pattern of 128 (ulp 1), giving 128 + q exactly; subtracting
+// 8 packed levels (element 2j low nibble) -> 4 words of bf16 pairs (q - zp) * s, in k
+// order.  Each nibble pair is spread into the two halves of a word with prmt, masked
+// and ORed with the bf16 pattern of 128 (ulp 1), giving 128 + q exactly; subtracting
 // 128 + zp is exact; the multiply by the bf16 scale rounds once.
-__device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t zz2, uint32_t s2) {
+__device__ __forceinline__ void dequant8(uint32_t x, uint32_t zz2, uint32_t s2, uint32_t *o) {
     const uint32_t x4 = x >> 4;
     const uint32_t magic = 0x43004300u, mask = 0x000F000Fu;
-    uint4 o;
-    o.x = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0400u), mask, magic), zz2), s2);
-    o.y = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0501u), mask, magic), zz2), s2);
-    o.z = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0602u), mask, magic), zz2), s2);
-    o.w = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0703u), mask, magic), zz2), s2);
-    return o;
+    o[0] = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0400u), mask, magic), zz2), s2);
+    o[1] = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0501u), mask, magic), zz2), s2);
+    o[2] = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0602u), mask, magic), zz2), s2);
+    o[3] = bf16x2_mul(bf16x2_sub(lop3_and_or(prmt(x, x4, 0x0703u), mask, magic), zz2), s2);
 }
 
 __device__ __forceinline__ uint32_t bf16_bits(float f) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
-    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 struct Params {
@@ -191,7 +204,8 @@ struct Params {
     const uint8_t *zeros;
     __nv_bfloat16 *Y;
     int M, N, K;
-    int vec_store;  // Y rows are 16-byte aligned (N % 8 == 0 and Y 16-byte aligned)
+    int mt;          // activation rows per tile (MMA N): multiple of 16, <= 256
+    uint32_t idesc;  // instruction descriptor for (M = 128, N = mt)
     WaitParams wait;
 };
 
@@ -202,41 +216,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Align the shared-window offset (not the generic address) to 1024 bytes, as the
     // 128-byte swizzle pattern of TMA and of the MMA descriptors assumes.
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sA = smem + OFF_A;
-    uint8_t *sBd = smem + OFF_BD;
-    uint8_t *sBq = smem + OFF_BQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *full_ab = bars;
-    uint64_t *empty_ab = full_ab + SA;
-    uint64_t *full_d = empty_ab + SA;
-    uint64_t *empty_d = full_d + SD;
-    uint64_t *tmem_full = empty_d + SD;
-    uint64_t *tmem_empty = tmem_full + 2;
-    uint64_t *mma_done = tmem_empty + 2;
+    uint64_t *full_ab = bars;          // activations + packed W landed (TMA)
+    uint64_t *empty_ab = full_ab + SA;  // stage consumed (MMA commit + dequant warps)
+    uint64_t *a_full = empty_ab + SA;   // TMEM A stage written (dequant warps)
+    uint64_t *a_empty = a_full + ST;    // TMEM A stage consumed (MMA commit)
+    uint64_t *acc_full = a_empty + ST;  // accumulator complete (MMA commit)
+    uint64_t *acc_empty = acc_full + 2;  // accumulator drained (epilogue warps)
+    uint64_t *mma_done = acc_empty + 2;
     uint64_t *never = mma_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m_tiles = (p.M + BM - 1) / BM;
-    const int n_tiles = (p.N + BN - 1) / BN;
+    const int mt = p.mt;
+    const int m_tiles = (p.M + mt - 1) / mt;
+    const int n_tiles = (p.N + BW - 1) / BW;
     const int num_tiles = m_tiles * n_tiles;
     const int KB = p.K / BK;
+    const int num_acc = (mt <= 128) ? 2 : 1;
     const unsigned long long tmo = p.wait.timeout_ns;
+    const int act_bytes = mt * BK * 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
             mbar_init(&full_ab[s], 1);
             mbar_init(&empty_ab[s], 1 + NUM_DEQ_WARPS);
         }
-        for (int s = 0; s < SD; ++s) {
-            mbar_init(&full_d[s], NUM_DEQ_WARPS);
-            mbar_init(&empty_d[s], 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&a_full[s], NUM_DEQ_WARPS);
+            mbar_init(&a_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&tmem_full[s], 1);
-            mbar_init(&tmem_empty[s], 4);
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], NUM_EPI_WARPS);
         }
         mbar_init(mma_done, 1);
         mbar_init(never, 1);
@@ -266,16 +280,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int mt = tile % m_tiles, nt = tile / m_tiles;
+                const int mi = tile % m_tiles, ni = tile / m_tiles;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty_ab[stage], phase ^ 1u, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_ab[stage], A_STAGE + BQ_STAGE);
-                    tma_load_2d(sA + stage * A_STAGE, &tmA, &full_ab[stage], kb * BK, mt * BM, pol);
-                    tma_load_2d(sBq + stage * BQ_STAGE, &tmB, &full_ab[stage], kb * (BK / 2),
-                                nt * BN, pol);
+                    uint8_t *st = smem + OFF_STAGES + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_ab[stage], act_bytes + BQ_STAGE);
+                    tma_load_2d(st, &tmA, &full_ab[stage], kb * BK, mi * mt, pol);
+                    tma_load_2d(st + ACT_STAGE_MAX, &tmB, &full_ab[stage], kb * (BK / 2), ni * BW, pol);
 #pragma unroll
                     for (int s = 0; s < SA; ++s)
                         if (s == static_cast<int>(stage)) issued_parity[s] = static_cast<int>(phase);
@@ -297,43 +311,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, dstage = 0, dphase = 0, acc = 0, acc_phase = 0;
+            uint32_t stage = 0, phase = 0, as = 0, aphase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             if (p.wait.stall) ok = mbar_wait(never, 0, abort_flag, tmo);  // test hook
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, tmo)) {
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + acc * 128u;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&full_ab[stage], phase, abort_flag, tmo) ||
-                        !mbar_wait(&full_d[dstage], dphase, abort_flag, tmo)) {
+                        !mbar_wait(&a_full[as], aphase, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_addr(sA + stage * A_STAGE);
-                    const uint32_t b_addr = smem_addr(sBd + dstage * BD_STAGE);
+                    const uint32_t b_addr = smem_addr(smem + OFF_STAGES + stage * STAGE_BYTES);
+                    const uint32_t a_tmem = tmem_base + ACC_COLS + as * A_COLS;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                                  kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_tmem_a(d_tmem, a_tmem + kk * 8, sw128_desc(b_addr + kk * 32), p.idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(&empty_ab[stage]);
-                    umma_commit(&empty_d[dstage]);
+                    umma_commit(&a_empty[as]);
                     if (++stage == SA) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (++dstage == SD) {
-                        dstage = 0;
-                        dphase ^= 1u;
+                    if (++as == ST) {
+                        as = 0;
+                        aphase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(&tmem_full[acc]);
-                if (++acc == 2) {
+                umma_commit(&acc_full[acc]);
+                if (++acc == static_cast<uint32_t>(num_acc)) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -343,59 +357,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_wait_drain(mma_done, 0, tmo);
         }
         __syncwarp();
-    } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
-        // ---------------- epilogue: TMEM -> bf16 -> global ----------------
-        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
+        // ---------------- epilogue: TMEM -> bf16 -> Y ----------------
+        const int quarter = warp & 3;                  // TMEM lanes [32q, 32q + 32)
+        const int half = (warp - EPI_WARP0) >> 2;      // which half of the tile's columns
+        const int cols = mt >> 1;                      // columns per half (multiple of 8)
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int mt = tile % m_tiles, nt = tile / m_tiles;
-            if (!warp_wait(&tmem_full[acc], acc_phase, abort_flag, tmo)) break;
+            const int mi = tile % m_tiles, ni = tile / m_tiles;
+            if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, tmo)) break;
             tc_fence_after();
-            const int gm = mt * BM + quarter * 32 + lane;
-            __nv_bfloat16 *yrow = p.Y + static_cast<int64_t>(gm) * p.N;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   acc * 128u + static_cast<uint32_t>(half * cols);
+            const int n = ni * BW + quarter * 32 + lane;
+            const int m0 = mi * mt + half * cols;
+            unsigned short *y = reinterpret_cast<unsigned short *>(p.Y) + n;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c0 = 0; c0 < cols; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + c, v);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (c0 + 8 * j < cols) tmem_ld_8cols(tbase + c0 + 8 * j, v + 8 * j);
                 tmem_wait_ld();
-                const int gn = nt * BN + c;
-                if (gm < p.M && gn < p.N) {
-                    if (p.vec_store && gn + 32 <= p.N) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + gn);
+                if (n < p.N) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                                pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (gn + j < p.N) yrow[gn + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = m0 + c0 + j;
+                        if (c0 + j < cols && m < p.M)
+                            y[static_cast<int64_t>(m) * p.N] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
                     }
                 }
             }
+            // Every warp has read its part: the accumulator may be reused.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tmem_empty[acc]);
-            if (++acc == 2) {
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (++acc == static_cast<uint32_t>(num_acc)) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
     } else if (warp >= DEQ_WARP0) {
-        // ---------------- dequantize packed W -> swizzled bf16 ----------------
-        const int r = threadIdx.x - DEQ_WARP0 * 32;  // tile row owned by this thread
+        // ---------------- dequantize packed W -> TMEM A stages ----------------
+        const int quarter = warp & 3;
+        const int half = (warp - DEQ_WARP0) >> 2;      // which 32 of the 64 k of a stage
+        const int r = quarter * 32 + lane;             // tile row owned by this thread
         const int ng = p.K / 128;
-        uint32_t stage = 0, phase = 0, dstage = 0, dphase = 0;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t stage = 0, phase = 0, as = 0, aphase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const int nt = tile / m_tiles;
-            const int n = nt * BN + r;
+            const int ni = tile / m_tiles;
+            const int n = ni * BW + r;
             const bool valid = n < p.N;
             const int64_t sz_row = static_cast<int64_t>(n) * ng;
             // Scales / zero points run two groups ahead of use.
-            uint32_t s_cur = 0, z_cur = 0, s_nx1 = 0, z_nx1 = 0, s_nx2 = 0, z_nx2 = 0;
+            uint32_t s_nx1 = 0, z_nx1 = 0, s_nx2 = 0, z_nx2 = 0;
             if (valid) {
                 s_nx1 = __half_as_ushort(p.scales[sz_row]);
                 z_nx1 = p.zeros[sz_row];
@@ -408,8 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < KB; ++kb) {
                 if ((kb & 1) == 0) {
                     const int g = kb >> 1;
-                    s_cur = s_nx1;
-                    z_cur = z_nx1;
+                    const uint32_t s_cur = s_nx1, z_cur = z_nx1;
                     s_nx1 = s_nx2;
                     z_nx1 = z_nx2;
                     if (valid && g + 2 < ng) {
@@ -428,31 +445,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint4 *src = reinterpret_cast<const uint4 *>(sBq + stage * BQ_STAGE + r * 32);
-                const uint4 w0 = src[0], w1 = src[1];
+                const uint4 w = *reinterpret_cast<const uint4 *>(
+                    smem + OFF_STAGES + stage * STAGE_BYTES + ACT_STAGE_MAX + r * 32 + half * 16);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_ab[stage]);
-                if (!warp_wait(&empty_d[dstage], dphase ^ 1u, abort_flag, tmo)) {
+                if (!warp_wait(&a_empty[as], aphase ^ 1u, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
-                uint8_t *row_base = sBd + dstage * BD_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
-                const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 o = dequant8(words[c], zz2, s2);
-                    *reinterpret_cast<uint4 *>(row_base + ((c ^ (r & 7)) << 4)) = o;
-                }
-                fence_proxy_async_smem();
+                uint32_t o[16];
+                dequant8(w.x, zz2, s2, o);
+                dequant8(w.y, zz2, s2, o + 4);
+                dequant8(w.z, zz2, s2, o + 8);
+                dequant8(w.w, zz2, s2, o + 12);
+                tmem_st_16cols(tmem_base + lane_addr + ACC_COLS + as * A_COLS + half * 16, o);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_d[dstage]);
+                if (lane == 0) mbar_arrive(&a_full[as]);
                 if (++stage == SA) {
                     stage = 0;
                     phase ^= 1u;
                 }
-                if (++dstage == SD) {
-                    dstage = 0;
-                    dphase ^= 1u;
+                if (++as == ST) {
+                    as = 0;
+                    aphase ^= 1u;
                 }
             }
         }
@@ -502,11 +519,12 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
                                __nv_bfloat16 *Y, cudaStream_t stream, int sms, WaitParams wp) {
     using namespace gemm;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return W4_ERR_UNSUPPORTED;
+    const int mt = static_cast<int>(M >= MT_MAX ? MT_MAX : ((M + 15) / 16) * 16);
     CUtensorMap tmA, tmB;
-    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, BK, BM,
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, BK, mt,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return W4_ERR_CUDA;
-    if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, K / 2, N, K / 2, BK / 2, BN,
+    if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, K / 2, N, K / 2, BK / 2, BW,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4_ERR_CUDA;
 
@@ -521,7 +539,7 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     });
     if (attr_err[dev] != cudaSuccess) return W4_ERR_CUDA;
 
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t tiles = ((M + mt - 1) / mt) * ((N + BW - 1) / BW);
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     Params prm;
     prm.scales = scales;
@@ -530,7 +548,8 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     prm.M = static_cast<int>(M);
     prm.N = static_cast<int>(N);
     prm.K = static_cast<int>(K);
-    prm.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(Y) & 15) == 0) ? 1 : 0;
+    prm.mt = mt;
+    prm.idesc = make_idesc(static_cast<uint32_t>(mt));
     prm.wait = wp;
 
     cudaLaunchConfig_t cfg = {};
