@@ -8,7 +8,9 @@ entries x10, group 128; A bf16 [1, 4096] ~ N(0, 1)); other workloads via --workl
 value      algorithmic GB/s of the whole step (quantize bytes W + qweight + scales +
            zeros, plus matmul bytes qweight + scales + zeros + A + Y) over the step's
            device time (CUDA events on the launching stream), inputs resident in HBM,
-           L2 flushed (256 MiB device write) before every step, outside the events.
+           L2 flushed (256 MiB device write, then read back so that no dirty line is
+           left to drain inside the next timed kernel) before every step, outside the
+           events.
 roofline   the kernel with the largest share of the step: its algorithmic bytes (or
            flops for the tensor-core GEMM) per launch over its average event-timed
            launch duration, against the measured HBM (or bf16) peak.
@@ -236,14 +238,22 @@ def run_ours(args, ws, rank, local, dist):
     z = torch.empty((N, K // 128), dtype=torch.uint8, device=dev)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        # Write a buffer twice the size of L2, then read it back: the write evicts
+        # every line, the read forces the dirty lines back to HBM here, outside the
+        # timed events, instead of during the next timed kernel.
+        flush.zero_()
+        torch.sum(flush, dim=0, out=sink)
 
     def step():
         w4.quantize_pack(Wd, out=(q, s, z), stream=stream)
         w4.matmul(Ad, q, s, z, out=Y, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize(dev)
 
@@ -253,7 +263,7 @@ def run_ours(args, ws, rank, local, dist):
     torch.cuda.synchronize(dev)
     sampler.start()
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[i][0].record(stream)
         w4.quantize_pack(Wd, out=(q, s, z), stream=stream)
         ev[i][1].record(stream)
@@ -333,7 +343,7 @@ def run_ours(args, ws, rank, local, dist):
             "workload": f"{args.workload}: {wl.desc}; group 128",
             "N": N, "K": K, "M": M, "group": 128, "w_dtype": wl.w_dtype,
             "step": "w4_quantize_pack + w4_matmul",
-            "l2": "flushed before every step (256 MiB device write, outside the timed events)",
+            "l2": "flushed before every step (256 MiB device write then read, outside the timed events)",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
         "roofline": roofline,

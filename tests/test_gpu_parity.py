@@ -163,6 +163,35 @@ def test_matmul_small_m_ragged(env, N, K, M):
     assert_matmul_ok(env, A, q, s, z)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("N,K", [(1, 2048), (37, 4096), (300, 8192), (1031, 2048), (9, 6144)])
+def test_matmul_streaming_gemv(env, M, N, K):
+    """Shapes that take the streaming GEMV (K a multiple of 2048): activations in
+    registers for M * ceil(K/4096) <= 2, in shared memory otherwise; N tails."""
+    import synth
+    _, _, orc = env
+    W, A = synth.make_random(N, K, M, seed=7 * N + K + M)
+    q, s, z = orc.quantize_pack(W)
+    assert_matmul_ok(env, A, q, s, z)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+def test_matmul_streaming_zero_rows(env, M):
+    """Rows of W that are all zero reconstruct to 0 exactly, so those outputs must be
+    exactly 0 on the streaming path too; other rows stay within tolerance."""
+    import synth
+    _, _, orc = env
+    W, A = synth.make_random(40, 4096, M, seed=11 + M)
+    W[3] = 0
+    W[17:25] = 0
+    q, s, z = orc.quantize_pack(W)
+    Yb = run_matmul(env, A, q, s, z)
+    assert np.all(Yb[:, 3] == 0) and np.all(Yb[:, 17:25] == 0)
+    Yref, S = orc.matmul(A, q, s, z)
+    ok, worst, idx = orc.check_y(Yb, Yref, S)
+    assert ok, (worst, idx)
+
+
 @pytest.mark.parametrize("name", ["tiny", "llama7b_gemv", "skinny_m8", "mlp70b"])
 def test_matmul_full_workloads_small_m(env, name):
     import synth

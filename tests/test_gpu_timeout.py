@@ -1,5 +1,7 @@
-"""Failure detection without a GPU fault: the tensor-core kernel's consumer is made to
-wait on a barrier that nothing signals; the bounded wait must run out, record
+"""Failure detection without a GPU fault: the consumers of the tensor-core kernel
+(M = 64) and of the streaming GEMV (M = 1: activations in registers; M = 3:
+activations in shared memory) are made to wait on a barrier that nothing
+signals; the bounded wait must run out, record
 W4_ERR_TIMEOUT in the device error word, drain its copies, free tensor memory and
 exit.  The context must stay usable (a normal call afterwards is correct)."""
 import numpy as np
@@ -8,13 +10,14 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def test_injected_stall_times_out_and_context_survives(oracle_mod):
+@pytest.mark.parametrize("M", [1, 3, 64])
+def test_injected_stall_times_out_and_context_survives(oracle_mod, M):
     import torch
     import synth
     from w4a16_matmul_asym_b300 import build
     build.build()
     import w4a16_matmul_asym_b300 as w4
-    W, A = synth.make_random(512, 1024, 64, seed=77)
+    W, A = synth.make_random(512, 2048, M, seed=77)
     q, s, z = oracle_mod.quantize_pack(W)
     Ad = torch.from_numpy(A.view(np.int16)).cuda().view(torch.bfloat16)
     qd, sd, zd = (torch.from_numpy(x).cuda() for x in (q, s, z))

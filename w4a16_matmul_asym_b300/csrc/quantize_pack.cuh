@@ -11,25 +11,28 @@
 //
 // Layout: the flat group index G = n * (K/128) + g addresses every output directly:
 // qweight bytes [64 G, 64 G + 64), scales[G], zeros[G], and W elements
-// [128 G, 128 G + 128).  So the kernel walks groups as one flat array.
+// [128 G, 128 G + 128).  The kernel walks groups as one flat array.
 //
-// Mapping: a half-warp owns a group; each lane holds 8 consecutive elements (one
-// 16-byte load for fp16, two for fp32).  A warp iteration covers 8 groups (2 KB of
-// fp16 W), with all four 512-byte warp loads issued before any is consumed.  Min and
-// max come from an 8-element local pass plus a 4-step xor-shuffle across the half
-// warp; each lane then writes its 8 nibbles as one 32-bit word, so a warp stores
-// 128 contiguous bytes per pair of groups.
+// Mapping: LPG lanes own a group (2 for fp16, 4 for fp32), each lane 128 contiguous
+// bytes of W (64 fp16 or 32 fp32 elements) read with eight 16-byte loads; a warp
+// iteration covers 4 KB of W.  The loads of the next iteration are issued before the
+// current one is processed.  Min/max: a local tree (on packed halves for fp16) and a
+// 1- or 2-step xor-shuffle.  Each lane writes its packed nibbles as 16- or 32-byte
+// vector stores; a warp stores 1 KB (fp16) or 512 B (fp32) of qweight contiguously.
 //
-// Quotient w/s without a divide per element: t = w * fl(1/s) lies within 3 ulp of the
-// IEEE quotient x = fl(w/s) (two roundings of 2^-24 relative each, plus x's own).
-// For |t| <= 64 that is below 2^-16, so whenever t is farther than 2^-16 from a
-// half-integer, rhe(t) == rhe(x).  Only elements inside that window (about 3e-5 of
-// them) take the IEEE division __fdiv_rn.  Elements with |t| > 31.5 clip to level 0
-// or 15 whichever integer they round to, so their rounding needs no care.
-// Rounding to an integer uses the add-1.5*2^23 trick: for |t| < 2^22,
-// fl(t + 1.5*2^23) = 1.5*2^23 + rhe(t) exactly; adding zp into the constant first is
-// exact too, and outside ties rhe(t + zp) == rhe(t) + zp.  The level is then the low
-// 4 bits of the clamped float's bit pattern.
+// The quotient w/s without a divide per element: t = w * fl(1/s) lies within 3 ulp
+// of the IEEE quotient x = fl(w/s) (two roundings of 2^-24 relative each, plus x's
+// own).  For |t| <= 64 that is below 2^-16, so whenever t is farther than 2^-16 from
+// a half-integer, rhe(t) == rhe(x) and no tie can occur.  Elements inside that
+// window (about 3e-5 of them) redo the word with the IEEE division __fdiv_rn.
+// Elements with |t| > 31.5 clip to level 0 or 15 whatever integer they round to.
+//   tie test: with M = 1.5 * 2^23, fl(t + M + zp) - (M + zp) = rhe(t) exactly for
+//             |t| < 2^22, so e = t - rhe(t) is exact.
+//   level:    lv = sat((t + zp) / 15) with one fma.sat; outside the tie window the
+//             rounding of fl(15 lv + M) - M is that of t + zp (the fma's errors stay
+//             below 6e-6 < 2^-16) and the saturation performs the clip to [0, 15].
+//   packing:  four levels per fp32 lane of an f32x2 pair, 2^23 + q0 + 16 q1 + 256 q2
+//             + 4096 q3 (exact), the two 16-bit sums merged with one prmt.
 #pragma once
 
 #include "common.cuh"
@@ -37,48 +40,145 @@
 namespace w4 {
 
 constexpr float kRoundMagic = 12582912.0f;              // 1.5 * 2^23
-constexpr uint32_t kRoundMagicBits = 0x4B400000u;       // bit pattern of kRoundMagic
 constexpr float kHalfMinusSlack = 0.4999847412109375f;  // 0.5 - 2^-16
 
+// ---- f32x2 helpers (Blackwell packed fp32) ------------------------------------------
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+    float d;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// Exact fp16 -> fp32 widening on the FMA pipe: f32(h) + (-0).
+__device__ __forceinline__ float widen_lo(uint32_t h2) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, 0f80000000;\n\t}"
+        : "=f"(r) : "r"(h2));
+    return r;
+}
+__device__ __forceinline__ float widen_hi(uint32_t h2) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, 0f80000000;\n\t}"
+        : "=f"(r) : "r"(h2));
+    return r;
+}
+
 struct GroupParams {
-    float s;       // fp32 scale
-    float rcp;     // fl(1/s)
-    float mz;      // kRoundMagic + zp (exact)
-    float zp;      // zero point as float (0..15)
+    float s;        // fp32 scale
+    uint64_t rcp2;  // (fl(1/s), fl(1/s))
+    uint64_t mz2;   // (M + zp, M + zp), exact
+    float r15;      // fl(1/15)
+    float c15;      // fl(zp * fl(1/15))
+    float zp;       // zero point (0..15) as float
 };
 
 __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
     GroupParams p;
     p.s = (mx == mn) ? 1.0f : __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-    const float zq = rintf(__fdiv_rn(-mn, p.s));
+    const float x = __fdiv_rn(-mn, p.s);
+    // rhe(x) for |x| < 2^22 via the magic add; larger |x| clips anyway.
+    const float zq = (fabsf(x) < 4194304.0f) ? __fsub_rn(__fadd_rn(x, kRoundMagic), kRoundMagic) : x;
     p.zp = fminf(fmaxf(zq, 0.0f), 15.0f);
-    p.rcp = __frcp_rn(p.s);
-    p.mz = __fadd_rn(kRoundMagic, p.zp);
+    const float rcp = __frcp_rn(p.s);
+    const float mz = __fadd_rn(kRoundMagic, p.zp);
+    p.rcp2 = f2pack(rcp, rcp);
+    p.mz2 = f2pack(mz, mz);
+    p.r15 = 0.0666666701436042785644531f;  // fl(1/15)
+    p.c15 = __fmul_rn(p.zp, p.r15);
     return p;
 }
 
-// Returns kRoundMagic + clip(rhe(w / s) + zp, 0, 15) as a float (bits 0x4B40000q).
-__device__ __forceinline__ float quantize_one(float w, const GroupParams &p) {
-    const float t = __fmul_rn(w, p.rcp);
-    float v = __fadd_rn(t, p.mz);
-    const float e = __fsub_rn(t, __fsub_rn(v, p.mz));
-    if (fabsf(e) > kHalfMinusSlack) {
-        // Near a half-integer: take the IEEE quotient and round it half-to-even.
-        const float x = __fdiv_rn(w, p.s);
-        const float k = __fsub_rn(__fadd_rn(x, kRoundMagic), kRoundMagic);  // rhe(x), |x| < 2^22
-        v = (fabsf(x) < 4194304.0f) ? __fadd_rn(kRoundMagic, __fadd_rn(k, p.zp)) : __fadd_rn(x, p.mz);
+// Exact reference for one element: kRoundMagic + clip(rhe(w / s) + zp, 0, 15).
+__device__ __forceinline__ float level_exact(float w, const GroupParams &p) {
+    const float x = __fdiv_rn(w, p.s);
+    float v;
+    if (fabsf(x) < 4194304.0f) {
+        const float k = __fsub_rn(__fadd_rn(x, kRoundMagic), kRoundMagic);  // rhe(x)
+        v = __fadd_rn(kRoundMagic, __fadd_rn(k, p.zp));
+    } else {
+        v = (x > 0.0f) ? kRoundMagic + 15.0f : kRoundMagic;
     }
     return fminf(fmaxf(v, kRoundMagic), kRoundMagic + 15.0f);
 }
 
-// Packs 8 levels (each as the float kRoundMagic + q) into one 32-bit word, element i
-// in bits [4i, 4i+4): sum_i (bits_i - magic) * 16^i, computed mod 2^32.
-__device__ __forceinline__ uint32_t pack8(const float (&v)[8]) {
-    uint32_t acc = 0u - kRoundMagicBits * 0x11111111u;
+// 8 consecutive elements w[0..7] -> one 32-bit word of nibbles (element i in bits
+// [4i, 4i+4)).  Pairs are (w[j], w[j+4]) so that one f32x2 packing chain builds the
+// low and the high 16 bits at once.
+__device__ __forceinline__ uint32_t quantize8(const float (&w)[8], const GroupParams &p) {
+    const uint64_t M2 = f2pack(kRoundMagic, kRoundMagic);
+    const uint64_t M22 = f2pack(4194304.0f, 4194304.0f);  // 2^22: L - 2^22 = 2^23 + q
+    const uint64_t c15x2 = f2pack(15.0f, 15.0f);
+    uint64_t t[4];
+    bool tie = false;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc += __float_as_uint(v[i]) * (1u << (4 * i));
-    return acc;
+    for (int j = 0; j < 4; ++j) {
+        t[j] = f2mul(f2pack(w[j], w[j + 4]), p.rcp2);
+        const uint64_t v = f2add(t[j], p.mz2);
+        const uint64_t e = f2sub(t[j], f2sub(v, p.mz2));
+        float elo, ehi;
+        f2unpack(e, elo, ehi);
+        tie |= (fabsf(elo) > kHalfMinusSlack) | (fabsf(ehi) > kHalfMinusSlack);
+    }
+    uint64_t q[4];
+    if (!tie) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float tlo, thi;
+            f2unpack(t[j], tlo, thi);
+            const uint64_t lv = f2pack(fma_sat(tlo, p.r15, p.c15), fma_sat(thi, p.r15, p.c15));
+            q[j] = f2fma(lv, c15x2, M2);            // M + level
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) q[j] = f2pack(level_exact(w[j], p), level_exact(w[j + 4], p));
+    }
+    // q[j] = M + level; element 0 pair takes M - 2^23 off so the chain carries 2^23.
+    uint64_t acc = f2sub(q[0], M22);
+    acc = f2fma(f2sub(q[1], M2), f2pack(16.0f, 16.0f), acc);
+    acc = f2fma(f2sub(q[2], M2), f2pack(256.0f, 256.0f), acc);
+    acc = f2fma(f2sub(q[3], M2), f2pack(4096.0f, 4096.0f), acc);
+    float lo, hi;
+    f2unpack(acc, lo, hi);
+    uint32_t word;
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(word) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+    return word;
 }
+
+template <bool kF32>
+struct QuantCfg {
+    static constexpr int kLanesPerGroup = kF32 ? 4 : 2;
+    static constexpr int kElemsPerLane = 128 / kLanesPerGroup;   // 32 or 64
+    static constexpr int kGroupsPerWarp = 32 / kLanesPerGroup;   // 8 or 16
+    static constexpr int kLoads = 8;                             // 16-byte loads per lane
+    static constexpr int kWords = kElemsPerLane / 8;             // output words per lane
+};
 
 template <bool kF32>
 __global__ void __launch_bounds__(256) quantize_pack_kernel(const void *__restrict__ W,
@@ -86,75 +186,100 @@ __global__ void __launch_bounds__(256) quantize_pack_kernel(const void *__restri
                                                             uint32_t *__restrict__ qw,
                                                             __half *__restrict__ scales,
                                                             uint8_t *__restrict__ zeros) {
+    using C = QuantCfg<kF32>;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;  // which group of a pair this lane works on
-    const int sub = lane & 15;   // 8-element slice of the group
+    const int gsub = lane / C::kLanesPerGroup;     // group within the warp's block
+    const int part = lane % C::kLanesPerGroup;     // slice of the group
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const char *wbytes = static_cast<const char *>(W);
 
-    for (int64_t base = warp * 8; base < total_groups; base += nwarps * 8) {
-        uint4 raw[4][kF32 ? 2 : 1];
-        // Issue all loads of the iteration first.
+    auto load = [&](int64_t base, uint4 (&r)[C::kLoads]) {
+        const int64_t g = base + gsub;
+        if (g < total_groups) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(wbytes + g * (kF32 ? 512 : 256) + part * 128);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t g = base + 2 * j + half;
-            const int64_t e = g * 128 + sub * 8;
-            if (g < total_groups) {
-                if constexpr (kF32) {
-                    const float *Wf = static_cast<const float *>(W);
-                    raw[j][0] = ldg_stream_16(Wf + e);
-                    raw[j][1] = ldg_stream_16(Wf + e + 4);
-                } else {
-                    raw[j][0] = ldg_stream_16(static_cast<const __half *>(W) + e);
-                }
-            } else {
+            for (int i = 0; i < C::kLoads; ++i) r[i] = __ldg(src + i);
+        } else {
 #pragma unroll
-                for (int u = 0; u < (kF32 ? 2 : 1); ++u) raw[j][u] = make_uint4(0, 0, 0, 0);
-            }
+            for (int i = 0; i < C::kLoads; ++i) r[i] = make_uint4(0, 0, 0, 0);
         }
+    };
+
+    int64_t base = warp * C::kGroupsPerWarp;
+    const int64_t stride = nwarps * C::kGroupsPerWarp;
+    uint4 nxt[C::kLoads];
+    if (base < total_groups) load(base, nxt);
+    for (; base < total_groups; base += stride) {
+        uint4 cur[C::kLoads];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t g = base + 2 * j + half;
+        for (int i = 0; i < C::kLoads; ++i) cur[i] = nxt[i];
+        if (base + stride < total_groups) load(base + stride, nxt);
+        const int64_t g = base + gsub;
+
+        // ---- min / max over the group ----
+        float mn, mx;
+        if constexpr (kF32) {
+            const float *f = reinterpret_cast<const float *>(cur);
+            mn = f[0];
+            mx = f[0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) {
+                mn = fminf(mn, f[i]);
+                mx = fmaxf(mx, f[i]);
+            }
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        } else {
+            const __half2 *h = reinterpret_cast<const __half2 *>(cur);
+            __half2 lo2 = __hmin2(h[0], h[1]), hi2 = __hmax2(h[0], h[1]);
+#pragma unroll
+            for (int i = 2; i < 32; i += 2) {
+                lo2 = __hmin2(lo2, __hmin2(h[i], h[i + 1]));
+                hi2 = __hmax2(hi2, __hmax2(h[i], h[i + 1]));
+            }
+            // (min, -max) in one half2 so one shuffle + one hmin2 combines both.
+            const __half mnh = __hmin(__low2half(lo2), __high2half(lo2));
+            const __half mxh = __hmax(__low2half(hi2), __high2half(hi2));
+            __half2 pk = __halves2half2(mnh, __hneg(mxh));
+            const uint32_t pku = *reinterpret_cast<const uint32_t *>(&pk);
+            const uint32_t oth = __shfl_xor_sync(0xffffffffu, pku, 1);
+            pk = __hmin2(pk, *reinterpret_cast<const __half2 *>(&oth));
+            const uint32_t pkb = *reinterpret_cast<const uint32_t *>(&pk);
+            mn = widen_lo(pkb);
+            mx = -widen_hi(pkb);
+        }
+        const GroupParams p = group_params(mn, mx);
+
+        // ---- quantize and pack, 8 elements per output word ----
+        uint32_t words[C::kWords];
+#pragma unroll
+        for (int c = 0; c < C::kWords; ++c) {
             float w[8];
-            float mn, mx;
             if constexpr (kF32) {
-                const float *f = reinterpret_cast<const float *>(&raw[j][0]);
+                const float *f = reinterpret_cast<const float *>(cur) + 8 * c;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) w[i] = f[i];
-                mn = fminf(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])),
-                           fminf(fminf(w[4], w[5]), fminf(w[6], w[7])));
-                mx = fmaxf(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])),
-                           fmaxf(fmaxf(w[4], w[5]), fmaxf(w[6], w[7])));
             } else {
-                const __half2 *h = reinterpret_cast<const __half2 *>(&raw[j][0]);
-                // min/max on packed halves (exact), then widen the two survivors.
-                const __half2 lo = __hmin2(__hmin2(h[0], h[1]), __hmin2(h[2], h[3]));
-                const __half2 hi = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
-                mn = fminf(__low2float(lo), __high2float(lo));
-                mx = fmaxf(__low2float(hi), __high2float(hi));
+                const uint32_t *u = reinterpret_cast<const uint32_t *>(cur) + 4 * c;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 f = __half22float2(h[i]);
-                    w[2 * i] = f.x;
-                    w[2 * i + 1] = f.y;
+                    w[2 * i] = widen_lo(u[i]);
+                    w[2 * i + 1] = widen_hi(u[i]);
                 }
             }
+            words[c] = quantize8(w, p);
+        }
+        if (g < total_groups) {
+            uint4 *dst = reinterpret_cast<uint4 *>(qw + g * 16 + part * C::kWords);
 #pragma unroll
-            for (int o = 8; o; o >>= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            }
-            const GroupParams p = group_params(mn, mx);
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = quantize_one(w[i], p);
-            const uint32_t word = pack8(v);
-            if (g < total_groups) {
-                qw[g * 16 + sub] = word;
-                if (sub == 0) {
-                    scales[g] = __float2half_rn(p.s);
-                    zeros[g] = static_cast<uint8_t>(p.zp);
-                }
+            for (int c = 0; c < C::kWords; c += 4)
+                dst[c / 4] = make_uint4(words[c], words[c + 1], words[c + 2], words[c + 3]);
+            if (part == 0) {
+                scales[g] = __float2half_rn(p.s);
+                zeros[g] = static_cast<uint8_t>(p.zp);
             }
         }
     }

@@ -5,7 +5,9 @@
 // enqueue it on the caller's stream with cudaLaunchKernelEx (whose return value is
 // the launch status); they never synchronize and never allocate.
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "gemm_tcgen05.cuh"
@@ -61,9 +63,53 @@ int launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
     return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-int launch_gemv(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const uint8_t *qweight,
-                const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y,
-                cudaStream_t stream, int sms) {
+// Persistent grid for the quantize kernel: enough 256-thread blocks to cover the
+// groups once, capped at the number that can be resident on every SM at once.
+template <typename Kern>
+dim3 quantize_grid(Kern kern, int64_t total_groups, int groups_per_warp, int sms) {
+    static std::once_flag once[kMaxDevices];
+    static int cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::call_once(once[dev], [&]() {
+        int per = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, 256, 0) != cudaSuccess || per < 1)
+            per = 1;
+        cached[dev] = per;
+    });
+    const int per_sm = cached[dev];
+    const int64_t per_block = static_cast<int64_t>(groups_per_warp) * 8;
+    int64_t blocks = (total_groups + per_block - 1) / per_block;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    if (blocks > cap) blocks = cap;
+    return dim3(static_cast<unsigned>(blocks));
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device (and per size).
+int ensure_smem_attr(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    int &have = done[{dev, kernel}];
+    if (have >= bytes) return W4_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return W4_ERR_CUDA;
+    have = bytes;
+    return W4_OK;
+}
+
+template <typename Kern>
+int launch_gemv_kernel(Kern kern, int threads, const CUtensorMap &tmS, const CUtensorMap &tmZ,
+                       const w4::gemv::Params &prm, int64_t grid, size_t smem, cudaStream_t stream) {
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(smem))) return rc;
+    return launch(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, tmS, tmZ, prm);
+}
+
+int launch_gemv_simple(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const uint8_t *qweight,
+                       const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y,
+                       cudaStream_t stream, int sms) {
     constexpr int R = 2;
     const int64_t warps_needed = (N + R - 1) / R;
     int64_t blocks = (warps_needed + 7) / 8;
@@ -79,6 +125,82 @@ int launch_gemv(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const u
         case 6: return launch(w4::gemv_simple_kernel<6, R>, grid, block, 0, stream, A, qweight, scales, zeros, Y, N, K);
         case 7: return launch(w4::gemv_simple_kernel<7, R>, grid, block, 0, stream, A, qweight, scales, zeros, Y, N, K);
         case 8: return launch(w4::gemv_simple_kernel<8, R>, grid, block, 0, stream, A, qweight, scales, zeros, Y, N, K);
+        default: return W4_ERR_INVALID_ARG;
+    }
+}
+
+constexpr size_t kGemvSmemLimit = 220 * 1024;
+
+// M <= 8.  The streaming kernels need the scales / zero points reachable by 2-D tensor
+// copies (K a multiple of 2048, 16-byte aligned tables, K <= 32768); otherwise the
+// plain kernel runs.  Activations in registers when M * ceil(K / 4096) <= 2, in shared
+// memory otherwise (if they fit).
+int launch_gemv(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const uint8_t *qweight,
+                const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y,
+                cudaStream_t stream, int sms, w4::WaitParams wp) {
+    namespace gv = w4::gemv;
+    const int64_t ng = K / 128;
+    const bool tma_ok = (K % 2048 == 0) && K <= 32768 && aligned(scales, 16) && aligned(zeros, 16) &&
+                        N <= INT32_MAX / 2;
+    const int64_t gpl = (ng + 31) / 32;
+    const bool rega = tma_ok && M * gpl <= 2;
+    // 16 consumer warps when a lane's activations take 64 registers, 8 when 128.
+    const int cw = (rega && M * gpl == 1) ? gv::CW_REGA : gv::CW_SMEMA;
+    size_t smem = kGemvSmemLimit + 1;
+    int stages = 0;
+    if (tma_ok) {
+        const int64_t sb = gv::stage_bytes(static_cast<int>(K), cw);
+        stages = static_cast<int>(gv::RING_BYTES / sb);
+        if (stages > gv::MAX_STAGES) stages = gv::MAX_STAGES;
+        if (!rega) {
+            const size_t fixed = gv::smem_bytes_smema(static_cast<int>(M), static_cast<int>(K), 0);
+            const int64_t room = static_cast<int64_t>(kGemvSmemLimit) - static_cast<int64_t>(fixed);
+            if (stages > room / sb) stages = static_cast<int>(room / sb);
+        }
+        if (stages >= 2)
+            smem = rega ? gv::smem_bytes_rega(static_cast<int>(K), stages, cw)
+                        : gv::smem_bytes_smema(static_cast<int>(M), static_cast<int>(K), stages);
+    }
+    if (!tma_ok || stages < 2 || smem > kGemvSmemLimit)
+        return launch_gemv_simple(A, M, N, K, qweight, scales, zeros, Y, stream, sms);
+
+    CUtensorMap tmS, tmZ;
+    if (!w4::gemm::make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, ng, N, ng * 2,
+                               static_cast<uint32_t>(ng), cw, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !w4::gemm::make_map_2d(&tmZ, CU_TENSOR_MAP_DATA_TYPE_UINT8, zeros, ng, N, ng,
+                               static_cast<uint32_t>(ng), cw, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4_ERR_CUDA;
+
+    // Contiguous bands of rows, at most one CTA per SM.
+    int64_t grid = (N + cw - 1) / cw;
+    if (grid > sms) grid = sms;
+    const int64_t per_cta = (N + grid - 1) / grid;
+    grid = (N + per_cta - 1) / per_cta;
+
+    gv::Params prm;
+    prm.A = A;
+    prm.qweight = qweight;
+    prm.Y = Y;
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.rows_per_cta = static_cast<int>(per_cta);
+    prm.stages = stages;
+    prm.wait = wp;
+    const int tr = gv::num_threads(gv::CW_REGA), ts = gv::num_threads(gv::CW_SMEMA);
+    if (rega) {
+        if (M == 1 && gpl == 1) return launch_gemv_kernel(gv::gemv_rega_kernel<1, 1, gv::CW_REGA>, tr, tmS, tmZ, prm, grid, smem, stream);
+        if (M == 1 && gpl == 2) return launch_gemv_kernel(gv::gemv_rega_kernel<1, 2, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        if (M == 2 && gpl == 1) return launch_gemv_kernel(gv::gemv_rega_kernel<2, 1, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+    }
+    switch (M) {
+        case 1: return launch_gemv_kernel(gv::gemv_smema_kernel<1, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 2: return launch_gemv_kernel(gv::gemv_smema_kernel<2, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 3: return launch_gemv_kernel(gv::gemv_smema_kernel<3, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 4: return launch_gemv_kernel(gv::gemv_smema_kernel<4, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 5: return launch_gemv_kernel(gv::gemv_smema_kernel<5, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 6: return launch_gemv_kernel(gv::gemv_smema_kernel<6, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 7: return launch_gemv_kernel(gv::gemv_smema_kernel<7, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
+        case 8: return launch_gemv_kernel(gv::gemv_smema_kernel<8, gv::CW_SMEMA>, ts, tmS, tmZ, prm, grid, smem, stream);
         default: return W4_ERR_INVALID_ARG;
     }
 }
@@ -112,16 +234,17 @@ int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, int group
     if (int rc = current_sm_count(&sms)) return rc;
 
     const int64_t total_groups = N * (K / W4_GROUP_SIZE);
-    // 8 groups per warp iteration, 8 warps per block; at most 8 resident blocks per SM.
-    int64_t blocks = (total_groups + 63) / 64;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    const dim3 grid(static_cast<unsigned>(blocks)), block(256);
     uint32_t *qw = reinterpret_cast<uint32_t *>(qweight);
     __half *sc = static_cast<__half *>(scales);
-    if (w_dtype == W4_DTYPE_F16)
-        return launch(w4::quantize_pack_kernel<false>, grid, block, 0, stream, W, total_groups, qw, sc, zeros);
-    return launch(w4::quantize_pack_kernel<true>, grid, block, 0, stream, W, total_groups, qw, sc, zeros);
+    const dim3 block(256);
+    if (w_dtype == W4_DTYPE_F16) {
+        auto kern = w4::quantize_pack_kernel<false>;
+        const dim3 grid = quantize_grid(kern, total_groups, w4::QuantCfg<false>::kGroupsPerWarp, sms);
+        return launch(kern, grid, block, 0, stream, W, total_groups, qw, sc, zeros);
+    }
+    auto kern = w4::quantize_pack_kernel<true>;
+    const dim3 grid = quantize_grid(kern, total_groups, w4::QuantCfg<true>::kGroupsPerWarp, sms);
+    return launch(kern, grid, block, 0, stream, W, total_groups, qw, sc, zeros);
 }
 
 int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const uint8_t *qweight,
@@ -143,7 +266,7 @@ int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const u
     const __nv_bfloat16 *a = static_cast<const __nv_bfloat16 *>(A);
     const __half *s = static_cast<const __half *>(scales);
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(Y);
-    if (M <= 8) return launch_gemv(a, M, N, K, qweight, s, zeros, y, stream, sms);
+    if (M <= 8) return launch_gemv(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
     return w4::launch_gemm_tcgen05(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
 }
 
