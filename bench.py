@@ -137,7 +137,8 @@ def barrier(dist):
 
 # ---- clocks ---------------------------------------------------------------------------
 class ClockSampler:
-    """Samples SM clock and clock-event (throttle) reasons through NVML while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons while running:
+    through NVML if it loads, else by polling nvidia-smi."""
 
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -148,43 +149,69 @@ class ClockSampler:
 
     def __init__(self, device_index: int, period_s: float = 0.01):
         self.period = period_s
+        self.index = device_index
         self.samples, self.reasons = [], set()
         self.max_mhz = None
+        self.error = None
+        self.source = None
         self._stop = threading.Event()
         self._thread = None
+        self.nv = None
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
+            self.nv = pynvml
+            self.source = "nvml"
+        except Exception as e:  # fall back to nvidia-smi
+            self.error = f"nvml: {type(e).__name__}: {e}"
+            self.source = "nvidia-smi"
+
+    def _sample_nvml(self):
+        self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+        bits = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        for b, name in self.REASONS.items():
+            if bits & b:
+                self.reasons.add(name)
+
+    def _sample_smi(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=5).stdout.strip().split(",")
+        self.samples.append(float(out[0]))
+        self.max_mhz = float(out[1])
+        for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                              "sw_power_cap"), out[2:]):
+            if val.strip().lower() == "active":
+                self.reasons.add(name)
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                bits = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for b, name in self.REASONS.items():
-                    if bits & b:
-                        self.reasons.add(name)
-            except Exception:
-                pass
+                self._sample_nvml() if self.nv is not None else self._sample_smi()
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
             time.sleep(self.period)
 
     def start(self):
-        if self.nv is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
 
     def stop(self):
         if self._thread is not None:
             self._stop.set()
             self._thread.join()
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples), "source": self.source}
+        if self.error:
+            out["note"] = self.error
+        return out
 
 
 # ---- CPU oracle timing --------------------------------------------------------------------
