@@ -192,6 +192,77 @@ def test_matmul_streaming_zero_rows(env, M):
     assert ok, (worst, idx)
 
 
+def _bf16_bits(x):
+    import synth
+    return synth.f32_to_bf16_bits(np.ascontiguousarray(x, np.float32))
+
+
+@pytest.mark.parametrize("K", [2048, 4096, 8192])
+def test_gemv_wide_range_activations(env, K):
+    """Activations whose groups each hold one huge element (2^20) next to values 2^-10
+    N(0, 1): every other element lies more than 12 binades below its group maximum,
+    so the decode GEMV cannot give it an exact integer digit and must carry it as a
+    residual (more than four per lane: the slow path).  The weight under each huge
+    element is 0, so it reconstructs to exactly 0 and the huge element contributes
+    nothing: the tolerance (relative to sum |a * w_hat|) is set by the small ones."""
+    import synth
+    _, _, orc = env
+    rng = np.random.default_rng(K + 5)
+    N = 77
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    a = (rng.standard_normal(K) * 2.0 ** -10).astype(np.float32)
+    big = np.arange(0, K, 128) + rng.integers(0, 128, K // 128)
+    a[big] = 2.0 ** 20
+    W[:, big] = 0
+    q, s, z = orc.quantize_pack(W)
+    A = _bf16_bits(a[None, :])
+    assert_matmul_ok(env, A, q, s, z)
+
+
+@pytest.mark.parametrize("K", [2048, 4096, 8192])
+def test_gemv_few_small_activations(env, K):
+    """One to three elements per group far below the group maximum (the register
+    residual list of the decode GEMV), mixed with exact zeros and subnormals."""
+    import synth
+    _, _, orc = env
+    rng = np.random.default_rng(K + 9)
+    N = 300
+    W, _ = synth.make_random(N, K, 1, seed=K + 9)
+    a = rng.standard_normal(K).astype(np.float32)
+    for g in range(K // 128):
+        idx = g * 128 + rng.choice(128, size=rng.integers(1, 4), replace=False)
+        a[idx] *= 2.0 ** -20
+    a[rng.integers(0, K, 8)] = 0.0
+    a[rng.integers(0, K, 4)] = 3e-39  # subnormal in bf16
+    q, s, z = orc.quantize_pack(W)
+    A = _bf16_bits(a[None, :])
+    assert_matmul_ok(env, A, q, s, z)
+
+
+@pytest.mark.parametrize("special", ["inf", "nan"])
+def test_gemv_nonfinite_activation(env, special):
+    """An infinite or NaN activation propagates as IEEE arithmetic would: a row whose
+    reconstructed weight there is 0 gives NaN (inf * 0), others give +-inf (or NaN)."""
+    import synth
+    torch, _, orc = env
+    K, N = 4096, 64
+    W, _ = synth.make_random(N, K, 1, seed=21)
+    rng = np.random.default_rng(21)
+    a = rng.standard_normal(K).astype(np.float32)
+    a[1000] = np.inf if special == "inf" else np.nan
+    W[:10, 1000] = 0  # these rows reconstruct 0 there
+    q, s, z = orc.quantize_pack(W)
+    A = _bf16_bits(a[None, :])
+    Yb = run_matmul(env, A, q, s, z)[0]
+    y = orc.bf16_bits_to_f64(Yb)
+    w_hat = orc.dequantize(q, s, z, K)
+    with np.errstate(invalid="ignore", over="ignore"):
+        ref = w_hat @ orc.bf16_bits_to_f64(A[0])
+    assert np.array_equal(np.isnan(y), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(y[fin], ref[fin])  # both +-inf
+
+
 @pytest.mark.parametrize("name", ["tiny", "llama7b_gemv", "skinny_m8", "mlp70b"])
 def test_matmul_full_workloads_small_m(env, name):
     import synth

@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "gemm_tcgen05.cuh"
 #include "gemv.cuh"
+#include "gemv_dp4a.cuh"
 #include "quantize_pack.cuh"
 
 namespace {
@@ -131,6 +132,56 @@ int launch_gemv_simple(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, 
 
 constexpr size_t kGemvSmemLimit = 220 * 1024;
 
+// M = 1 on integer dot products: K a multiple of 2048 up to 16384, 16-byte aligned
+// scales and zero points.  Returns W4_ERR_UNSUPPORTED for other shapes.
+int launch_gemv_dp4a(const __nv_bfloat16 *A, int64_t N, int64_t K, const uint8_t *qweight,
+                     const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y, cudaStream_t stream,
+                     int sms, w4::WaitParams wp) {
+    namespace gd = w4::gemv_dp4a;
+    if (K % 2048 != 0 || K > 16384 || !aligned(scales, 16) || !aligned(zeros, 16) || N > INT32_MAX / 2)
+        return W4_ERR_UNSUPPORTED;
+    const int k = static_cast<int>(K), ng = k / 128;
+    // A lane owns a 128-group (half of one when K = 2048); WR warps share a row, WR
+    // the smallest divisor of the consumer-warp count covering the row's pieces.
+    const int H = ng >= 32 ? 1 : 2;
+    int WR = 1;
+    while (WR <= gd::CW && (32 * WR < H * ng || gd::CW % WR != 0)) ++WR;
+    if (WR > gd::CW) return W4_ERR_UNSUPPORTED;
+    int stages = 0, smem = 0;
+    for (int s = gd::MAX_STAGES; s >= 2; --s) {
+        const int total = H == 1 ? gd::Layout<1>(k, WR, s).total : gd::Layout<2>(k, WR, s).total;
+        if (total <= gd::SMEM_LIMIT) {
+            stages = s;
+            smem = total;
+            break;
+        }
+    }
+    if (stages == 0) return W4_ERR_UNSUPPORTED;
+    gd::Params prm;
+    prm.A = A;
+    prm.qweight = qweight;
+    prm.scales = scales;
+    prm.zeros = zeros;
+    prm.Y = Y;
+    prm.N = static_cast<int>(N);
+    prm.K = k;
+    prm.WR = WR;
+    prm.stages = stages;
+    prm.wait = wp;
+    int64_t grid = N < sms ? N : sms;
+    const int64_t per_cta = (N + grid - 1) / grid;
+    grid = (N + per_cta - 1) / per_cta;
+    prm.rows_per_cta = static_cast<int>(per_cta);
+    if (H == 1) {
+        auto kern = gd::w4a16_gemv_dp4a_kernel<1>;
+        if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
+        return launch(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
+    }
+    auto kern = gd::w4a16_gemv_dp4a_kernel<2>;
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
+    return launch(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
+}
+
 // M <= 8.  The streaming kernels need the scales / zero points reachable by 2-D tensor
 // copies (K a multiple of 2048, 16-byte aligned tables, K <= 32768); otherwise the
 // plain kernel runs.  Activations in registers when M * ceil(K / 4096) <= 2, in shared
@@ -139,6 +190,10 @@ int launch_gemv(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const u
                 const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y,
                 cudaStream_t stream, int sms, w4::WaitParams wp) {
     namespace gv = w4::gemv;
+    if (M == 1) {
+        const int rc = launch_gemv_dp4a(A, N, K, qweight, scales, zeros, Y, stream, sms, wp);
+        if (rc != W4_ERR_UNSUPPORTED) return rc;
+    }
     const int64_t ng = K / 128;
     const bool tma_ok = (K % 2048 == 0) && K <= 32768 && aligned(scales, 16) && aligned(zeros, 16) &&
                         N <= INT32_MAX / 2;
