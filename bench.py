@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
     "quantize_pack": ["w4a16_matmul_asym_b300/csrc/quantize_pack.cuh"],
-    "gemv": ["w4a16_matmul_asym_b300/csrc/gemv.cuh"],
+    "gemv": ["w4a16_matmul_asym_b300/csrc/gemv_dp4a.cuh", "w4a16_matmul_asym_b300/csrc/gemv.cuh"],
     "gemm_tcgen05": ["w4a16_matmul_asym_b300/csrc/gemm_tcgen05.cuh"],
 }
 
