@@ -97,8 +97,13 @@ W4_API int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, in
  * (Architecture Overview and Step 2: dequantization fused with the matmul as the hot
  * path).  Accuracy contract, per output element:
  *     |Y - Y_exact| <= 8e-3 * sum_k |A[m,k] * W_hat[n,k]| + ulp_bf16(|Y_exact|) / 2.
- * Paths: M <= 8 runs a CUDA-core split-K GEMV; M >= 9 runs a tcgen05 tensor-core GEMM
- * (bf16 x bf16 -> fp32 in tensor memory) on tiles dequantized to bf16 in shared memory.
+ * Paths: M = 1 runs integer dot products (dp4a) on exact block-floating-point
+ * activation digits; 2 <= M <= 8 a CUDA-core split-K GEMV (bf16 x bf16 -> fp32 FMA);
+ * 9 <= M <= 16 with fewer 128-row tiles than three quarters of the SMs a tcgen05 kernel
+ * that splits K across tensor-memory lanes; otherwise a tcgen05 tensor-core GEMM
+ * (bf16 x bf16 -> fp32 in tensor memory) on weight tiles dequantized into tensor memory.
+ * Shapes a fast path cannot take (K not a multiple of 2048, unaligned scale or zero
+ * tables) run a plain CUDA-core kernel.
  *
  * Arguments:
  *   A        device pointer, bf16 [M, K]; 16-byte aligned.

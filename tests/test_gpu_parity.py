@@ -321,6 +321,18 @@ def test_matmul_gemm_shapes(env, M, N, K):
     assert_matmul_ok(env, A, q, s, z)
 
 
+@pytest.mark.parametrize("M,N,K", [(9, 37, 2048), (12, 300, 4096), (16, 4096, 4096), (13, 1031, 2048),
+                                   (10, 200, 8192), (16, 9, 6144)])
+def test_matmul_skinny_tensor_core(env, M, N, K):
+    """9 <= M <= 16 with few 128-row tiles and K a multiple of 2048: the kernel that
+    splits K across TMEM lanes (8 or 16 parts per row); odd M pads the B operand."""
+    import synth
+    _, _, orc = env
+    W, A = synth.make_random(N, K, M, seed=900 + M + N)
+    q, s, z = orc.quantize_pack(W)
+    assert_matmul_ok(env, A, q, s, z)
+
+
 @pytest.mark.parametrize("M", [9, 10, 12, 15, 16, 20])
 def test_matmul_gemm_small_m_tail(env, M):
     import synth

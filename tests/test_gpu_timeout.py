@@ -1,7 +1,7 @@
-"""Failure detection without a GPU fault: the consumers of the tensor-core kernel
-(M = 64) and of the streaming GEMV (M = 1: activations in registers; M = 3:
-activations in shared memory) are made to wait on a barrier that nothing
-signals; the bounded wait must run out, record
+"""Failure detection without a GPU fault: the consumers of the tensor-core GEMM
+(M = 64), of the split-K tensor-core kernel (M = 12), of the integer-dot decode GEMV
+(M = 1) and of the streaming GEMV with activations in shared memory (M = 3) are made
+to wait on a barrier that nothing signals; the bounded wait must run out, record
 W4_ERR_TIMEOUT in the device error word, drain its copies, free tensor memory and
 exit.  The context must stay usable (a normal call afterwards is correct)."""
 import numpy as np
@@ -10,7 +10,7 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M", [1, 3, 64])
+@pytest.mark.parametrize("M", [1, 3, 12, 64])
 def test_injected_stall_times_out_and_context_survives(oracle_mod, M):
     import torch
     import synth
