@@ -13,11 +13,14 @@
 // qweight bytes [64 G, 64 G + 64), scales[G], zeros[G], and W elements
 // [128 G, 128 G + 128).  The kernel walks groups as one flat array.
 //
-// Mapping: LPG lanes own a group (2 for fp16, 4 for fp32), each lane 128 contiguous
-// bytes of W (64 fp16 or 32 fp32 elements) read with eight 16-byte loads; a warp
-// iteration covers 4 KB of W.  The loads of the next iteration are issued before the
-// current one is processed.  Min/max: a local tree (on packed halves for fp16) and a
-// 1- or 2-step xor-shuffle.  Each lane writes its packed nibbles as 16- or 32-byte
+// Mapping: LPG lanes own a group (2 for fp16, 4 for fp32), each lane one 128-byte line
+// of W (64 fp16 or 32 fp32 elements).  One CTA per SM: a producer warp streams W
+// through a 3-stage shared-memory ring with 2-D tensor copies (64 KB per stage: one
+// 4 KB block per consumer warp), 128-byte swizzled so that the 8 lanes of a quarter
+// warp read 8 different bank groups; the 16 consumer warps copy their lines into
+// registers, release the stage at once and quantize from registers.  Up to 192 KB of
+// W is in flight per SM.  Min/max: a local tree (on packed halves for fp16) and a 1- or
+// 2-step xor-shuffle.  Each lane writes its packed nibbles as 16- or 32-byte
 // vector stores; a warp stores 1 KB (fp16) or 512 B (fp32) of qweight contiguously.
 //
 // The quotient w/s without a divide per element: t = w * fl(1/s) lies within 3 ulp
@@ -180,109 +183,192 @@ struct QuantCfg {
     static constexpr int kWords = kElemsPerLane / 8;             // output words per lane
 };
 
+// One lane's 128 bytes of W (cur, natural order) -> its qweight words; the group's
+// scale and zero point are written by the lane with part 0.  g = flat group index.
 template <bool kF32>
-__global__ void __launch_bounds__(256) quantize_pack_kernel(const void *__restrict__ W,
-                                                            int64_t total_groups,
-                                                            uint32_t *__restrict__ qw,
-                                                            __half *__restrict__ scales,
-                                                            uint8_t *__restrict__ zeros) {
+__device__ __forceinline__ void quantize_lane(const uint4 (&cur)[QuantCfg<kF32>::kLoads], int64_t g,
+                                              int part, int64_t total_groups, uint32_t *__restrict__ qw,
+                                              __half *__restrict__ scales, uint8_t *__restrict__ zeros) {
     using C = QuantCfg<kF32>;
-    const int lane = threadIdx.x & 31;
-    const int gsub = lane / C::kLanesPerGroup;     // group within the warp's block
-    const int part = lane % C::kLanesPerGroup;     // slice of the group
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const char *wbytes = static_cast<const char *>(W);
-
-    auto load = [&](int64_t base, uint4 (&r)[C::kLoads]) {
-        const int64_t g = base + gsub;
-        if (g < total_groups) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(wbytes + g * (kF32 ? 512 : 256) + part * 128);
+    // ---- min / max over the group ----
+    float mn, mx;
+    if constexpr (kF32) {
+        const float *f = reinterpret_cast<const float *>(cur);
+        mn = f[0];
+        mx = f[0];
 #pragma unroll
-            for (int i = 0; i < C::kLoads; ++i) r[i] = __ldg(src + i);
-        } else {
-#pragma unroll
-            for (int i = 0; i < C::kLoads; ++i) r[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 1; i < 32; ++i) {
+            mn = fminf(mn, f[i]);
+            mx = fmaxf(mx, f[i]);
         }
-    };
-
-    int64_t base = warp * C::kGroupsPerWarp;
-    const int64_t stride = nwarps * C::kGroupsPerWarp;
-    uint4 nxt[C::kLoads];
-    if (base < total_groups) load(base, nxt);
-    for (; base < total_groups; base += stride) {
-        uint4 cur[C::kLoads];
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    } else {
+        const __half2 *h = reinterpret_cast<const __half2 *>(cur);
+        __half2 lo2 = __hmin2(h[0], h[1]), hi2 = __hmax2(h[0], h[1]);
 #pragma unroll
-        for (int i = 0; i < C::kLoads; ++i) cur[i] = nxt[i];
-        if (base + stride < total_groups) load(base + stride, nxt);
-        const int64_t g = base + gsub;
+        for (int i = 2; i < 32; i += 2) {
+            lo2 = __hmin2(lo2, __hmin2(h[i], h[i + 1]));
+            hi2 = __hmax2(hi2, __hmax2(h[i], h[i + 1]));
+        }
+        // (min, -max) in one half2 so one shuffle + one hmin2 combines both.
+        const __half mnh = __hmin(__low2half(lo2), __high2half(lo2));
+        const __half mxh = __hmax(__low2half(hi2), __high2half(hi2));
+        __half2 pk = __halves2half2(mnh, __hneg(mxh));
+        const uint32_t pku = *reinterpret_cast<const uint32_t *>(&pk);
+        const uint32_t oth = __shfl_xor_sync(0xffffffffu, pku, 1);
+        pk = __hmin2(pk, *reinterpret_cast<const __half2 *>(&oth));
+        const uint32_t pkb = *reinterpret_cast<const uint32_t *>(&pk);
+        mn = widen_lo(pkb);
+        mx = -widen_hi(pkb);
+    }
+    const GroupParams p = group_params(mn, mx);
 
-        // ---- min / max over the group ----
-        float mn, mx;
+    // ---- quantize and pack, 8 elements per output word ----
+    uint32_t words[C::kWords];
+#pragma unroll
+    for (int c = 0; c < C::kWords; ++c) {
+        float w[8];
         if constexpr (kF32) {
-            const float *f = reinterpret_cast<const float *>(cur);
-            mn = f[0];
-            mx = f[0];
+            const float *f = reinterpret_cast<const float *>(cur) + 8 * c;
 #pragma unroll
-            for (int i = 1; i < 32; ++i) {
-                mn = fminf(mn, f[i]);
-                mx = fmaxf(mx, f[i]);
-            }
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            for (int i = 0; i < 8; ++i) w[i] = f[i];
         } else {
-            const __half2 *h = reinterpret_cast<const __half2 *>(cur);
-            __half2 lo2 = __hmin2(h[0], h[1]), hi2 = __hmax2(h[0], h[1]);
+            const uint32_t *u = reinterpret_cast<const uint32_t *>(cur) + 4 * c;
 #pragma unroll
-            for (int i = 2; i < 32; i += 2) {
-                lo2 = __hmin2(lo2, __hmin2(h[i], h[i + 1]));
-                hi2 = __hmax2(hi2, __hmax2(h[i], h[i + 1]));
+            for (int i = 0; i < 4; ++i) {
+                w[2 * i] = widen_lo(u[i]);
+                w[2 * i + 1] = widen_hi(u[i]);
             }
-            // (min, -max) in one half2 so one shuffle + one hmin2 combines both.
-            const __half mnh = __hmin(__low2half(lo2), __high2half(lo2));
-            const __half mxh = __hmax(__low2half(hi2), __high2half(hi2));
-            __half2 pk = __halves2half2(mnh, __hneg(mxh));
-            const uint32_t pku = *reinterpret_cast<const uint32_t *>(&pk);
-            const uint32_t oth = __shfl_xor_sync(0xffffffffu, pku, 1);
-            pk = __hmin2(pk, *reinterpret_cast<const __half2 *>(&oth));
-            const uint32_t pkb = *reinterpret_cast<const uint32_t *>(&pk);
-            mn = widen_lo(pkb);
-            mx = -widen_hi(pkb);
         }
-        const GroupParams p = group_params(mn, mx);
-
-        // ---- quantize and pack, 8 elements per output word ----
-        uint32_t words[C::kWords];
+        words[c] = quantize8(w, p);
+    }
+    if (g < total_groups) {
+        uint4 *dst = reinterpret_cast<uint4 *>(qw + g * 16 + part * C::kWords);
 #pragma unroll
-        for (int c = 0; c < C::kWords; ++c) {
-            float w[8];
-            if constexpr (kF32) {
-                const float *f = reinterpret_cast<const float *>(cur) + 8 * c;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = f[i];
-            } else {
-                const uint32_t *u = reinterpret_cast<const uint32_t *>(cur) + 4 * c;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w[2 * i] = widen_lo(u[i]);
-                    w[2 * i + 1] = widen_hi(u[i]);
-                }
-            }
-            words[c] = quantize8(w, p);
-        }
-        if (g < total_groups) {
-            uint4 *dst = reinterpret_cast<uint4 *>(qw + g * 16 + part * C::kWords);
-#pragma unroll
-            for (int c = 0; c < C::kWords; c += 4)
-                dst[c / 4] = make_uint4(words[c], words[c + 1], words[c + 2], words[c + 3]);
-            if (part == 0) {
-                scales[g] = __float2half_rn(p.s);
-                zeros[g] = static_cast<uint8_t>(p.zp);
-            }
+        for (int c = 0; c < C::kWords; c += 4)
+            dst[c / 4] = make_uint4(words[c], words[c + 1], words[c + 2], words[c + 3]);
+        if (part == 0) {
+            scales[g] = __float2half_rn(p.s);
+            zeros[g] = static_cast<uint8_t>(p.zp);
         }
     }
+}
+
+namespace quant {
+constexpr int CW = 16;                       // consumer warps
+constexpr int NUM_THREADS = (CW + 1) * 32;
+constexpr int STAGES = 3;
+constexpr int LINES = CW * 32;               // 128-byte lines per stage (one per consumer lane)
+constexpr int STAGE_BYTES = LINES * 128;     // 64 KB
+constexpr int BOX_LINES = 256;               // tensor-copy box: 128 B x 256 lines
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 1024;
+}  // namespace quant
+
+// W viewed as bytes in 128-byte lines: tmW is a 2-D map {128 B, total_lines} with
+// 128-byte swizzle.  Stage unit u covers lines [u * LINES, (u + 1) * LINES), i.e.
+// groups [u * CW * kGroupsPerWarp, ...); CTA b takes units b, b + gridDim.x, ...
+template <bool kF32>
+__global__ void __launch_bounds__(quant::NUM_THREADS, 1)
+    quantize_pack_kernel(const __grid_constant__ CUtensorMap tmW, int64_t total_groups,
+                         uint32_t *__restrict__ qw, __half *__restrict__ scales,
+                         uint8_t *__restrict__ zeros, WaitParams wait) {
+    using C = QuantCfg<kF32>;
+    using namespace quant;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *never = empty + STAGES;
+    __shared__ int abort_flag_s;
+    volatile int *abort_flag = &abort_flag_s;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const unsigned long long tmo = wait.timeout_ns;
+    constexpr int kLinesPerGroup = C::kLanesPerGroup;
+    const int64_t total_lines = total_groups * kLinesPerGroup;
+    const int64_t units = (total_lines + LINES - 1) / LINES;
+    const int64_t my_units = units > blockIdx.x ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        mbar_init(never, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmW);
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued_parity[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+            bool ok = true;
+            for (int64_t lt = 0; lt < my_units; ++lt) {
+                const int stage = static_cast<int>(lt % STAGES);
+                const uint32_t phase = static_cast<uint32_t>(lt / STAGES) & 1u;
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, tmo)) {
+                    ok = false;
+                    break;
+                }
+                const int64_t line0 = (blockIdx.x + lt * gridDim.x) * LINES;
+                // Boxes that start inside the tensor; a box reaching past its end is
+                // filled with zeros (and counts in full).
+                const int nbox = static_cast<int>(min(static_cast<int64_t>(LINES / BOX_LINES),
+                                                      (total_lines - line0 + BOX_LINES - 1) / BOX_LINES));
+                uint8_t *st = smem + stage * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nbox) * BOX_LINES * 128);
+                for (int b = 0; b < nbox; ++b)
+                    tma_load_2d(st + b * BOX_LINES * 128, &tmW, &full[stage], 0,
+                                static_cast<int>(line0 + b * BOX_LINES), pol);
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s)
+                    if (s == stage) issued_parity[s] = static_cast<int>(phase);
+            }
+            if (!ok) {
+                const unsigned long long t0 = globaltimer_ns();
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued_parity[s] < 0) continue;
+                    while (!mbar_try_wait(smem_addr(&full[s]), static_cast<uint32_t>(issued_parity[s])))
+                        if (globaltimer_ns() - t0 > tmo) break;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumers ----------------
+        const int gsub = lane / C::kLanesPerGroup;  // group within the warp's block
+        const int part = lane % C::kLanesPerGroup;  // line within the group
+        const int ln = warp * 32 + lane;             // my line within the stage
+        bool ok = true;
+        if (wait.stall) ok = mbar_wait(never, 0, abort_flag, tmo);  // test hook: nothing signals it
+        for (int64_t lt = 0; ok && lt < my_units; ++lt) {
+            const int stage = static_cast<int>(lt % STAGES);
+            const uint32_t phase = static_cast<uint32_t>(lt / STAGES) & 1u;
+            if (!mbar_wait(&full[stage], phase, abort_flag, tmo)) break;
+            // Logical 16-byte chunk i of line ln sits at chunk i ^ (ln & 7).
+            const uint8_t *line = smem + stage * STAGE_BYTES + ln * 128;
+            uint4 cur[C::kLoads];
+#pragma unroll
+            for (int i = 0; i < C::kLoads; ++i)
+                cur[i] = *reinterpret_cast<const uint4 *>(line + ((i ^ (ln & 7)) << 4));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            const int64_t g = ((blockIdx.x + lt * gridDim.x) * LINES) / kLinesPerGroup + warp * C::kGroupsPerWarp + gsub;
+            quantize_lane<kF32>(cur, g, part, total_groups, qw, scales, zeros);
+        }
+    }
+    __syncthreads();
 }
 
 }  // namespace w4

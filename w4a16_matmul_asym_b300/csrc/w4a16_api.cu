@@ -65,28 +65,6 @@ int launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
     return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-// Persistent grid for the quantize kernel: enough 256-thread blocks to cover the
-// groups once, capped at the number that can be resident on every SM at once.
-template <typename Kern>
-dim3 quantize_grid(Kern kern, int64_t total_groups, int groups_per_warp, int sms) {
-    static std::once_flag once[kMaxDevices];
-    static int cached[kMaxDevices];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
-    std::call_once(once[dev], [&]() {
-        int per = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, 256, 0) != cudaSuccess || per < 1)
-            per = 1;
-        cached[dev] = per;
-    });
-    const int per_sm = cached[dev];
-    const int64_t per_block = static_cast<int64_t>(groups_per_warp) * 8;
-    int64_t blocks = (total_groups + per_block - 1) / per_block;
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
-    if (blocks > cap) blocks = cap;
-    return dim3(static_cast<unsigned>(blocks));
-}
-
 // Raises a kernel's dynamic shared-memory limit once per device (and per size).
 int ensure_smem_attr(const void *kernel, int bytes) {
     static std::mutex mu;
@@ -338,15 +316,27 @@ int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, int group
     const int64_t total_groups = N * (K / W4_GROUP_SIZE);
     uint32_t *qw = reinterpret_cast<uint32_t *>(qweight);
     __half *sc = static_cast<__half *>(scales);
-    const dim3 block(256);
+    // W as bytes in 128-byte lines (2 per fp16 group, 4 per fp32 group), streamed by
+    // 128 x 256-line tensor copies with 128-byte swizzle.
+    const int lines_per_group = w_dtype == W4_DTYPE_F16 ? 2 : 4;
+    const int64_t total_lines = total_groups * lines_per_group;
+    if (total_lines >= (int64_t(1) << 31)) return W4_ERR_UNSUPPORTED;
+    CUtensorMap tmW;
+    if (!w4::gemm::make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, 128, static_cast<uint64_t>(total_lines), 128,
+                               128, w4::quant::BOX_LINES, CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_CUDA;
+    const int64_t units = (total_lines + w4::quant::LINES - 1) / w4::quant::LINES;
+    const dim3 grid(static_cast<unsigned>(units < sms ? units : sms));
+    const dim3 block(w4::quant::NUM_THREADS);
+    const w4::WaitParams wp = wait_params();
     if (w_dtype == W4_DTYPE_F16) {
         auto kern = w4::quantize_pack_kernel<false>;
-        const dim3 grid = quantize_grid(kern, total_groups, w4::QuantCfg<false>::kGroupsPerWarp, sms);
-        return launch(kern, grid, block, 0, stream, W, total_groups, qw, sc, zeros);
+        if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
+        return launch(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
     }
     auto kern = w4::quantize_pack_kernel<true>;
-    const dim3 grid = quantize_grid(kern, total_groups, w4::QuantCfg<true>::kGroupsPerWarp, sms);
-    return launch(kern, grid, block, 0, stream, W, total_groups, qw, sc, zeros);
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
+    return launch(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
 }
 
 int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const uint8_t *qweight,
