@@ -350,6 +350,31 @@ def test_matmul_gemm_zero_weights(env):
     assert np.all(run_matmul(env, A, q, s, z) == 0)
 
 
+@pytest.mark.parametrize("M,N,K,offset", [(200, 264, 256, 0), (300, 1000, 512, 0), (17, 4104, 256, 0),
+                                          (40, 136, 384, 1), (129, 257, 384, 0)])
+def test_matmul_gemm_output_guard(env, M, N, K, offset):
+    """Y placed inside a larger buffer keeps the elements around it untouched.  With
+    offset 0 and N % 8 == 0, Y is 16-byte aligned and the tensor-store epilogue writes
+    it (boxes clipped at N and M); offset 1 makes Y 2-byte aligned, as N % 8 != 0 does,
+    which selects direct stores."""
+    import synth
+    torch, w4, orc = env
+    W, A = synth.make_random(N, K, M, seed=M + 3 * N + K + offset)
+    q, s, z = orc.quantize_pack(W)
+    sentinel = 0x7F7B  # a bf16 NaN pattern the kernel never produces
+    pad = N + offset
+    buf = torch.full((pad + M * N + N,), sentinel, dtype=torch.int16, device="cuda")
+    Y = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+    w4.matmul(to_dev_bf16(torch, A), torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(),
+              torch.from_numpy(z).cuda(), out=Y)
+    torch.cuda.synchronize()
+    flat = buf.cpu().numpy().view(np.uint16)
+    assert np.all(flat[:pad] == sentinel) and np.all(flat[pad + M * N:] == sentinel)
+    Yref, S = orc.matmul(A, q, s, z)
+    ok, worst, idx = orc.check_y(flat[pad:pad + M * N].reshape(M, N), Yref, S)
+    assert ok, f"worst ratio {worst:.3g} at {idx}"
+
+
 def test_matmul_prefill_workload_sampled(env):
     """Full-size prefill workload (M=2048, N=14336, K=4096) in the launch configuration
     the benchmark times; checked on 6000 sampled outputs plus one full output row and

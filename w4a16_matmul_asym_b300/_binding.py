@@ -143,7 +143,13 @@ def matmul(A, qweight, scales, zeros, group: int = GROUP_SIZE, stream=None, out=
         raise TypeError("qweight/zeros must be uint8 and scales float16")
     if tuple(qweight.shape) != (N, K // 2):
         raise ValueError(f"qweight shape {tuple(qweight.shape)} does not match K={K}")
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    if out is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        if (out.dtype != torch.bfloat16 or tuple(out.shape) != (M, N) or not out.is_contiguous()
+                or out.device != A.device):
+            raise ValueError(f"out must be a contiguous bfloat16 tensor of shape ({M}, {N}) on {A.device}")
+        Y = out
     rc = w4_matmul(A.data_ptr(), M, N, K, group, qweight.data_ptr(), scales.data_ptr(),
                    zeros.data_ptr(), Y.data_ptr(), _stream_handle(stream))
     if rc != W4_OK:

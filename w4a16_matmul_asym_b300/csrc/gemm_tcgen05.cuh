@@ -19,19 +19,24 @@
 //   warp 0        TMA producer: activation tile [MT x 64] bf16 + packed W [128 x 32 B]
 //   warp 1        allocates all 512 TMEM columns; one lane issues the MMAs
 //   warps 4-11    epilogue: two warps per TMEM lane quarter, each draining half of the
-//                 accumulator columns, 32 at a time, to bf16 Y (one warp store writes
-//                 32 consecutive n of one row of Y)
+//                 accumulator columns, 32 at a time, to bf16.  The accumulator is handed
+//                 back to the MMA warp as soon as the last column is in registers; the
+//                 values go through a per-warp shared-memory block [m][32 n] and one TMA
+//                 tensor store per warp and tile, which runs under the next tile's MMAs
+//                 (direct 2-byte stores instead when Y's rows are not 16-byte aligned)
 //   warps 12-19   dequantize: two warps per lane quarter; thread = one row of the W
 //                 tile, 32 of its 64 k per k-block -> tcgen05.st into a TMEM A stage
 // TMEM: columns [0, 256) accumulators (two of 128 when MT <= 128, one of 256 otherwise),
 // columns [256, 512) eight A-operand stages of 32 columns (64 bf16 per lane).
-// Shared memory: 5 stages of (activation tile, packed W tile).
+// Shared memory: 4 stages of (activation tile, packed W tile), then the epilogue's
+// 8 x 8 KB store-staging blocks.
 // Every wait is bounded (see common.cuh); on a timeout the CTA drains its copies and
 // MMAs, frees TMEM and exits, leaving W4_ERR_TIMEOUT in the device error word.
 #pragma once
 
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -42,7 +47,7 @@ namespace gemm {
 constexpr int BW = 128;                       // W rows per tile (MMA M, TMEM lanes)
 constexpr int BK = 64;                        // k per stage
 constexpr int MT_MAX = 256;                   // activation rows per tile (MMA N), max
-constexpr int SA = 5;                         // (activation, packed W) smem stages
+constexpr int SA = 4;                         // (activation, packed W) smem stages
 constexpr int ST = 8;                         // TMEM A-operand stages
 constexpr int ACT_STAGE_MAX = MT_MAX * BK * 2;  // 32 KB
 constexpr int BQ_STAGE = BW * BK / 2;         // 4 KB
@@ -56,8 +61,11 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;            // accumulator region
 constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
 
+constexpr int Y_WARP_BYTES = (MT_MAX / 2) * 32 * 2;  // one epilogue warp's [m][32 n] bf16 block
+
 constexpr int OFF_STAGES = 0;
-constexpr int OFF_BAR = OFF_STAGES + SA * STAGE_BYTES;
+constexpr int OFF_YST = OFF_STAGES + SA * STAGE_BYTES;
+constexpr int OFF_BAR = OFF_YST + NUM_EPI_WARPS * Y_WARP_BYTES;
 constexpr int NUM_BARS = 2 * SA + 2 * ST + 4 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -206,12 +214,13 @@ struct Params {
     int M, N, K;
     int mt;          // activation rows per tile (MMA N): multiple of 16, <= 256
     uint32_t idesc;  // instruction descriptor for (M = 128, N = mt)
+    int tma_store;   // 1: Y written by TMA tensor stores (tmY valid), 0: direct stores
     WaitParams wait;
 };
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const Params p) {
+                      const __grid_constant__ CUtensorMap tmY, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     // Align the shared-window offset (not the generic address) to 1024 bytes, as the
     // 128-byte swizzle pattern of TMA and of the MMA descriptors assumes.
@@ -260,6 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (p.tma_store) prefetch_tensormap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -362,6 +372,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;                  // TMEM lanes [32q, 32q + 32)
         const int half = (warp - EPI_WARP0) >> 2;      // which half of the tile's columns
         const int cols = mt >> 1;                      // columns per half (multiple of 8)
+        // This warp's staging block: `cols` rows of m, 32 consecutive n (64 bytes) each.
+        unsigned short *ystage =
+            reinterpret_cast<unsigned short *>(smem + OFF_YST + (warp - EPI_WARP0) * Y_WARP_BYTES);
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int mi = tile % m_tiles, ni = tile / m_tiles;
@@ -372,6 +385,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int n = ni * BW + quarter * 32 + lane;
             const int m0 = mi * mt + half * cols;
             unsigned short *y = reinterpret_cast<unsigned short *>(p.Y) + n;
+            if (p.tma_store) {
+                // The previous tile's store out of this block has finished reading it.
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+            }
 #pragma unroll 1
             for (int c0 = 0; c0 < cols; c0 += 32) {
                 uint32_t v[32];
@@ -379,7 +397,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int j = 0; j < 4; ++j)
                     if (c0 + 8 * j < cols) tmem_ld_8cols(tbase + c0 + 8 * j, v + 8 * j);
                 tmem_wait_ld();
-                if (n < p.N) {
+                if (c0 + 32 >= cols) {
+                    // This warp's part of the accumulator is in registers: hand it back.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[acc]);
+                }
+                if (p.tma_store) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < cols)
+                            ystage[(c0 + j) * 32 + lane] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                } else if (n < p.N) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int m = m0 + c0 + j;
@@ -389,15 +419,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            // Every warp has read its part: the accumulator may be reused.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (p.tma_store) {
+                // Generic-proxy writes of every lane before the async-proxy read of the store.
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int x = ni * BW + quarter * 32;
+                if (lane == 0 && x < p.N && m0 < p.M) {
+                    tma_store_2d(&tmY, ystage, x, m0);  // clipped at N and M
+                    bulk_commit_group();
+                }
+                __syncwarp();
+            }
             if (++acc == static_cast<uint32_t>(num_acc)) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
+        // Stores issued by this warp complete before the CTA exits.
+        if (p.tma_store && lane == 0) bulk_wait_group0();
+        __syncwarp();
     } else if (warp >= DEQ_WARP0) {
         // ---------------- dequantize packed W -> TMEM A stages ----------------
         const int quarter = warp & 3;
@@ -527,6 +567,14 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, K / 2, N, K / 2, BK / 2, BW,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4_ERR_CUDA;
+    // Y by tensor stores when its base and row pitch are 16-byte aligned: box of 32 n
+    // (64 bytes) by mt / 2 rows of m, one per epilogue warp and tile.
+    CUtensorMap tmY;
+    memset(&tmY, 0, sizeof(tmY));
+    const bool tma_store = (reinterpret_cast<uintptr_t>(Y) & 15u) == 0 && (N % 8) == 0;
+    if (tma_store && !make_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, N * 2, 32,
+                                  static_cast<uint32_t>(mt / 2), CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4_ERR_CUDA;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return W4_ERR_CUDA;
@@ -550,6 +598,7 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     prm.K = static_cast<int>(K);
     prm.mt = mt;
     prm.idesc = make_idesc(static_cast<uint32_t>(mt));
+    prm.tma_store = tma_store ? 1 : 0;
     prm.wait = wp;
 
     cudaLaunchConfig_t cfg = {};
@@ -557,7 +606,7 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = stream;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel, tmA, tmB, prm);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel, tmA, tmB, tmY, prm);
     return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
