@@ -16,8 +16,11 @@
 // and every dequantized weight serves MT activation rows.
 //
 // One persistent CTA per SM, 640 threads (20 warps):
-//   warp 0        TMA producer: activation tile [MT x 64] bf16 + packed W [128 x 32 B]
+//   warp 0        TMA producer of the activation tiles [MT x 64] bf16
 //   warp 1        allocates all 512 TMEM columns; one lane issues the MMAs
+//   warp 2        TMA producer of the packed W tiles [128 x 32 B], on a ring of its own
+//                 so that dequantization runs ahead of the MMAs, bounded only by the
+//                 TMEM A stages, and its latency stays off the MMAs' path
 //   warps 4-11    epilogue: two warps per TMEM lane quarter, each draining half of the
 //                 accumulator columns, 32 at a time, to bf16.  The accumulator is handed
 //                 back to the MMA warp as soon as the last column is in registers; the
@@ -28,8 +31,8 @@
 //                 tile, 32 of its 64 k per k-block -> tcgen05.st into a TMEM A stage
 // TMEM: columns [0, 256) accumulators (two of 128 when MT <= 128, one of 256 otherwise),
 // columns [256, 512) eight A-operand stages of 32 columns (64 bf16 per lane).
-// Shared memory: 4 stages of (activation tile, packed W tile), then the epilogue's
-// 8 x 8 KB store-staging blocks.
+// Shared memory: 4 activation stages (32 KB), 8 packed-W stages (4 KB), then the
+// epilogue's 8 x 8 KB store-staging blocks.
 // Every wait is bounded (see common.cuh); on a timeout the CTA drains its copies and
 // MMAs, frees TMEM and exits, leaving W4_ERR_TIMEOUT in the device error word.
 #pragma once
@@ -47,11 +50,11 @@ namespace gemm {
 constexpr int BW = 128;                       // W rows per tile (MMA M, TMEM lanes)
 constexpr int BK = 64;                        // k per stage
 constexpr int MT_MAX = 256;                   // activation rows per tile (MMA N), max
-constexpr int SA = 4;                         // (activation, packed W) smem stages
+constexpr int SA = 4;                         // activation smem stages
+constexpr int SW = 8;                         // packed-W smem stages
 constexpr int ST = 8;                         // TMEM A-operand stages
 constexpr int ACT_STAGE_MAX = MT_MAX * BK * 2;  // 32 KB
 constexpr int BQ_STAGE = BW * BK / 2;         // 4 KB
-constexpr int STAGE_BYTES = ACT_STAGE_MAX + BQ_STAGE;
 constexpr int NUM_THREADS = 640;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
@@ -63,10 +66,11 @@ constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
 
 constexpr int Y_WARP_BYTES = (MT_MAX / 2) * 32 * 2;  // one epilogue warp's [m][32 n] bf16 block
 
-constexpr int OFF_STAGES = 0;
-constexpr int OFF_YST = OFF_STAGES + SA * STAGE_BYTES;
+constexpr int OFF_ACT = 0;
+constexpr int OFF_W = OFF_ACT + SA * ACT_STAGE_MAX;
+constexpr int OFF_YST = OFF_W + SW * BQ_STAGE;
 constexpr int OFF_BAR = OFF_YST + NUM_EPI_WARPS * Y_WARP_BYTES;
-constexpr int NUM_BARS = 2 * SA + 2 * ST + 4 + 2;
+constexpr int NUM_BARS = 2 * SA + 2 * SW + 2 * ST + 4 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
@@ -207,6 +211,51 @@ __device__ __forceinline__ uint32_t bf16_bits(float f) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
 }
 
+// One TMA producer thread: for each k-block of this CTA's tiles in order, waits for a
+// free stage of its ring and copies one box into it (activations: [mt x 64] at
+// (k, m); packed W: [128 x 32 B] at (k / 2, n)).  On an abort it waits for every copy
+// it issued to land before returning.
+template <int S, bool kW>
+__device__ __forceinline__ void produce(const CUtensorMap *map, uint8_t *ring, uint32_t stage_bytes,
+                                        uint32_t tx_bytes, uint64_t *full, uint64_t *empty,
+                                        int num_tiles, int m_tiles, int KB, int mt,
+                                        volatile int *abort_flag, unsigned long long tmo) {
+    const uint64_t pol = policy_evict_last();
+    int issued_parity[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) issued_parity[s] = -1;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int mi = tile % m_tiles, ni = tile / m_tiles;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, tmo)) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = ring + stage * stage_bytes;
+            mbar_arrive_expect_tx(&full[stage], tx_bytes);
+            if (kW)
+                tma_load_2d(st, map, &full[stage], kb * (BK / 2), ni * BW, pol);
+            else
+                tma_load_2d(st, map, &full[stage], kb * BK, mi * mt, pol);
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+                if (s == static_cast<int>(stage)) issued_parity[s] = static_cast<int>(phase);
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Drain: every copy this thread issued must land before the CTA exits.
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+            if (issued_parity[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_parity[s]), tmo);
+    }
+}
+
 struct Params {
     const __half *scales;
     const uint8_t *zeros;
@@ -226,9 +275,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // 128-byte swizzle pattern of TMA and of the MMA descriptors assumes.
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *full_ab = bars;          // activations + packed W landed (TMA)
-    uint64_t *empty_ab = full_ab + SA;  // stage consumed (MMA commit + dequant warps)
-    uint64_t *a_full = empty_ab + SA;   // TMEM A stage written (dequant warps)
+    uint64_t *act_full = bars;           // activation tile landed (TMA)
+    uint64_t *act_empty = act_full + SA;  // activation stage consumed (MMA commit)
+    uint64_t *w_full = act_empty + SA;    // packed W tile landed (TMA)
+    uint64_t *w_empty = w_full + SW;      // packed W stage read (dequant warps)
+    uint64_t *a_full = w_empty + SW;      // TMEM A stage written (dequant warps)
     uint64_t *a_empty = a_full + ST;    // TMEM A stage consumed (MMA commit)
     uint64_t *acc_full = a_empty + ST;  // accumulator complete (MMA commit)
     uint64_t *acc_empty = acc_full + 2;  // accumulator drained (epilogue warps)
@@ -250,8 +301,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&full_ab[s], 1);
-            mbar_init(&empty_ab[s], 1 + NUM_DEQ_WARPS);
+            mbar_init(&act_full[s], 1);
+            mbar_init(&act_empty[s], 1);
+        }
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], NUM_DEQ_WARPS);
         }
         for (int s = 0; s < ST; ++s) {
             mbar_init(&a_full[s], NUM_DEQ_WARPS);
@@ -281,42 +336,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_last();
-            int issued_parity[SA];
-#pragma unroll
-            for (int s = 0; s < SA; ++s) issued_parity[s] = -1;
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int mi = tile % m_tiles, ni = tile / m_tiles;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&empty_ab[stage], phase ^ 1u, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *st = smem + OFF_STAGES + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_ab[stage], act_bytes + BQ_STAGE);
-                    tma_load_2d(st, &tmA, &full_ab[stage], kb * BK, mi * mt, pol);
-                    tma_load_2d(st + ACT_STAGE_MAX, &tmB, &full_ab[stage], kb * (BK / 2), ni * BW, pol);
-#pragma unroll
-                    for (int s = 0; s < SA; ++s)
-                        if (s == static_cast<int>(stage)) issued_parity[s] = static_cast<int>(phase);
-                    if (++stage == SA) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // Drain: every copy this thread issued must land before the CTA exits.
-#pragma unroll
-                for (int s = 0; s < SA; ++s)
-                    if (issued_parity[s] >= 0)
-                        mbar_wait_drain(&full_ab[s], static_cast<uint32_t>(issued_parity[s]), tmo);
-            }
-        }
+        // ---------------- TMA producer: activations ----------------
+        if (lane == 0)
+            produce<SA, false>(&tmA, smem + OFF_ACT, ACT_STAGE_MAX, static_cast<uint32_t>(act_bytes),
+                               act_full, act_empty, num_tiles, m_tiles, KB, mt, abort_flag, tmo);
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------- TMA producer: packed W ----------------
+        if (lane == 0)
+            produce<SW, true>(&tmB, smem + OFF_W, BQ_STAGE, BQ_STAGE, w_full, w_empty, num_tiles, m_tiles,
+                              KB, mt, abort_flag, tmo);
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -332,19 +361,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * 128u;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&full_ab[stage], phase, abort_flag, tmo) ||
+                    if (!mbar_wait(&act_full[stage], phase, abort_flag, tmo) ||
                         !mbar_wait(&a_full[as], aphase, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_addr = smem_addr(smem + OFF_STAGES + stage * STAGE_BYTES);
+                    const uint32_t b_addr = smem_addr(smem + OFF_ACT + stage * ACT_STAGE_MAX);
                     const uint32_t a_tmem = tmem_base + ACC_COLS + as * A_COLS;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         umma_tmem_a(d_tmem, a_tmem + kk * 8, sw128_desc(b_addr + kk * 32), p.idesc,
                                     (kb | kk) != 0 ? 1u : 0u);
-                    umma_commit(&empty_ab[stage]);
+                    umma_commit(&act_empty[stage]);
                     umma_commit(&a_empty[as]);
                     if (++stage == SA) {
                         stage = 0;
@@ -445,7 +474,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = quarter * 32 + lane;             // tile row owned by this thread
         const int ng = p.K / 128;
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t stage = 0, phase = 0, as = 0, aphase = 0;
+        uint32_t ws = 0, wphase = 0, as = 0, aphase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             const int ni = tile / m_tiles;
@@ -481,14 +510,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     s2 = sb | (sb << 16);
                     zz2 = zb | (zb << 16);
                 }
-                if (!warp_wait(&full_ab[stage], phase, abort_flag, tmo)) {
+                if (!warp_wait(&w_full[ws], wphase, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
-                const uint4 w = *reinterpret_cast<const uint4 *>(
-                    smem + OFF_STAGES + stage * STAGE_BYTES + ACT_STAGE_MAX + r * 32 + half * 16);
+                const uint4 w =
+                    *reinterpret_cast<const uint4 *>(smem + OFF_W + ws * BQ_STAGE + r * 32 + half * 16);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_ab[stage]);
+                if (lane == 0) mbar_arrive(&w_empty[ws]);
                 if (!warp_wait(&a_empty[as], aphase ^ 1u, abort_flag, tmo)) {
                     ok = false;
                     break;
@@ -503,9 +532,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[as]);
-                if (++stage == SA) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (++ws == SW) {
+                    ws = 0;
+                    wphase ^= 1u;
                 }
                 if (++as == ST) {
                     as = 0;
