@@ -17,7 +17,8 @@
 //
 // One persistent CTA per SM, 640 threads (20 warps):
 //   warp 0        TMA producer of the activation tiles [MT x 64] bf16
-//   warp 1        allocates all 512 TMEM columns; one lane issues the MMAs
+//   warp 1        allocates all 512 TMEM columns and runs the MMA loop; one elected
+//                 lane issues the MMAs and their commits
 //   warp 2        TMA producer of the packed W tiles [128 x 32 B], on a ring of its own
 //                 so that dequantization runs ahead of the MMAs, bounded only by the
 //                 TMEM A stages, and its latency stays off the MMAs' path
@@ -28,7 +29,8 @@
 //                 tensor store per warp and tile, which runs under the next tile's MMAs
 //                 (direct 2-byte stores instead when Y's rows are not 16-byte aligned)
 //   warps 12-19   dequantize: two warps per lane quarter; thread = one row of the W
-//                 tile, 32 of its 64 k per k-block -> tcgen05.st into a TMEM A stage
+//                 tile, 32 of its 64 k of each k-block, one quantization group (two
+//                 k-blocks) per iteration -> tcgen05.st into two TMEM A stages
 // TMEM: columns [0, 256) accumulators (two of 128 when MT <= 128, one of 256 otherwise),
 // columns [256, 512) eight A-operand stages of 32 columns (64 bf16 per lane).
 // Shared memory: 4 activation stages (32 KB), 8 packed-W stages (4 KB), then the
@@ -63,6 +65,7 @@ constexpr int NUM_DEQ_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;            // accumulator region
 constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
+static_assert(SW % 2 == 0 && ST % 2 == 0, "dequantize warps take W and A stages in pairs");
 
 constexpr int Y_WARP_BYTES = (MT_MAX / 2) * 32 * 2;  // one epilogue warp's [m][32 n] bf16 block
 
@@ -121,6 +124,27 @@ __device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Warp-wide forms: every lane of a converged warp executes them (so the operands stay
+// warp-uniform) and elect.sync picks the one lane that issues, the same lane each time
+// for a fully active warp, so its commits track its own MMAs.
+__device__ __forceinline__ void umma_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_warp(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_addr(bar))
         : "memory");
 }
 // 16 consecutive 32-bit columns of this thread's TMEM lane <- registers.
@@ -349,52 +373,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, as = 0, aphase = 0, acc = 0, acc_phase = 0;
-            bool ok = true;
-            if (p.wait.stall) ok = mbar_wait(never, 0, abort_flag, tmo);  // test hook
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, tmo)) {
+        // The whole warp runs the loop; one elected lane issues the MMAs and commits.
+        uint32_t stage = 0, phase = 0, as = 0, aphase = 0, acc = 0, acc_phase = 0;
+        bool ok = true;
+        if (p.wait.stall) ok = warp_wait(never, 0, abort_flag, tmo);  // test hook
+        // Descriptor of activation stage 0; the start address field (bytes / 16) moves by
+        // ACT_STAGE_MAX / 16 per stage and by 2 per 16-k step.
+        const uint64_t bdesc0 = sw128_desc(smem_addr(smem + OFF_ACT));
+        const uint32_t idesc = p.idesc;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            if (!warp_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, tmo)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * 128u;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!warp_wait(&act_full[stage], phase, abort_flag, tmo) ||
+                    !warp_wait(&a_full[as], aphase, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * 128u;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&act_full[stage], phase, abort_flag, tmo) ||
-                        !mbar_wait(&a_full[as], aphase, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t b_addr = smem_addr(smem + OFF_ACT + stage * ACT_STAGE_MAX);
-                    const uint32_t a_tmem = tmem_base + ACC_COLS + as * A_COLS;
+                const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (ACT_STAGE_MAX >> 4));
+                const uint32_t a_tmem = tmem_base + ACC_COLS + as * A_COLS;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_tmem_a(d_tmem, a_tmem + kk * 8, sw128_desc(b_addr + kk * 32), p.idesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
-                    umma_commit(&act_empty[stage]);
-                    umma_commit(&a_empty[as]);
-                    if (++stage == SA) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                    if (++as == ST) {
-                        as = 0;
-                        aphase ^= 1u;
-                    }
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_tmem_a_warp(d_tmem, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                umma_commit_warp(&act_empty[stage]);
+                umma_commit_warp(&a_empty[as]);
+                if (++stage == SA) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
-                if (!ok) break;
-                umma_commit(&acc_full[acc]);
-                if (++acc == static_cast<uint32_t>(num_acc)) {
-                    acc = 0;
-                    acc_phase ^= 1u;
+                if (++as == ST) {
+                    as = 0;
+                    aphase ^= 1u;
                 }
             }
-            // All MMAs issued by this thread complete before TMEM is released.
-            umma_commit(mma_done);
-            mbar_wait_drain(mma_done, 0, tmo);
+            if (!ok) break;
+            umma_commit_warp(&acc_full[acc]);
+            if (++acc == static_cast<uint32_t>(num_acc)) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
+        // All MMAs issued by the elected lane complete before TMEM is released.
+        umma_commit_warp(mma_done);
+        if (lane == 0) mbar_wait_drain(mma_done, 0, tmo);
         __syncwarp();
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
         // ---------------- epilogue: TMEM -> bf16 -> Y ----------------
@@ -491,52 +517,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     z_nx2 = p.zeros[sz_row + 1];
                 }
             }
-            uint32_t s2 = 0, zz2 = 0;
-            for (int kb = 0; kb < KB; ++kb) {
-                if ((kb & 1) == 0) {
-                    const int g = kb >> 1;
-                    const uint32_t s_cur = s_nx1, z_cur = z_nx1;
-                    s_nx1 = s_nx2;
-                    z_nx1 = z_nx2;
-                    if (valid && g + 2 < ng) {
-                        s_nx2 = __half_as_ushort(p.scales[sz_row + g + 2]);
-                        z_nx2 = p.zeros[sz_row + g + 2];
-                    }
-                    // bf16(s16) twice, and 128 + zp (exact) twice; invalid rows give 0.
-                    const uint32_t sb = valid ? bf16_bits(__half2float(__ushort_as_half(
-                                                    static_cast<unsigned short>(s_cur))))
-                                              : 0u;
-                    const uint32_t zb = bf16_bits(128.0f + static_cast<float>(z_cur));
-                    s2 = sb | (sb << 16);
-                    zz2 = zb | (zb << 16);
+            // One quantization group (two k-blocks: W stages ws, ws + 1 and TMEM A stages
+            // as, as + 1, both rings of even length) per iteration.
+            for (int g = 0; g < ng; ++g) {
+                const uint32_t s_cur = s_nx1, z_cur = z_nx1;
+                s_nx1 = s_nx2;
+                z_nx1 = z_nx2;
+                if (valid && g + 2 < ng) {
+                    s_nx2 = __half_as_ushort(p.scales[sz_row + g + 2]);
+                    z_nx2 = p.zeros[sz_row + g + 2];
                 }
-                if (!warp_wait(&w_full[ws], wphase, abort_flag, tmo)) {
+                // bf16(s16) twice, and 128 + zp (exact) twice; invalid rows give 0.
+                const uint32_t sb =
+                    valid ? bf16_bits(__half2float(__ushort_as_half(static_cast<unsigned short>(s_cur))))
+                          : 0u;
+                const uint32_t zb = bf16_bits(128.0f + static_cast<float>(z_cur));
+                const uint32_t s2 = sb | (sb << 16);
+                const uint32_t zz2 = zb | (zb << 16);
+                if (!warp_wait(&w_full[ws], wphase, abort_flag, tmo) ||
+                    !warp_wait(&w_full[ws + 1], wphase, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
-                const uint4 w =
-                    *reinterpret_cast<const uint4 *>(smem + OFF_W + ws * BQ_STAGE + r * 32 + half * 16);
+                const uint8_t *wsrc = smem + OFF_W + ws * BQ_STAGE + r * 32 + half * 16;
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(wsrc);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(wsrc + BQ_STAGE);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&w_empty[ws]);
-                if (!warp_wait(&a_empty[as], aphase ^ 1u, abort_flag, tmo)) {
+                if (lane == 0) {
+                    mbar_arrive(&w_empty[ws]);
+                    mbar_arrive(&w_empty[ws + 1]);
+                }
+                if (!warp_wait(&a_empty[as], aphase ^ 1u, abort_flag, tmo) ||
+                    !warp_wait(&a_empty[as + 1], aphase ^ 1u, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
+                const uint32_t dst = tmem_base + lane_addr + ACC_COLS + as * A_COLS + half * 16;
                 uint32_t o[16];
-                dequant8(w.x, zz2, s2, o);
-                dequant8(w.y, zz2, s2, o + 4);
-                dequant8(w.z, zz2, s2, o + 8);
-                dequant8(w.w, zz2, s2, o + 12);
-                tmem_st_16cols(tmem_base + lane_addr + ACC_COLS + as * A_COLS + half * 16, o);
+                dequant8(w0.x, zz2, s2, o);
+                dequant8(w0.y, zz2, s2, o + 4);
+                dequant8(w0.z, zz2, s2, o + 8);
+                dequant8(w0.w, zz2, s2, o + 12);
+                tmem_st_16cols(dst, o);
+                dequant8(w1.x, zz2, s2, o);
+                dequant8(w1.y, zz2, s2, o + 4);
+                dequant8(w1.z, zz2, s2, o + 8);
+                dequant8(w1.w, zz2, s2, o + 12);
+                tmem_st_16cols(dst + A_COLS, o);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[as]);
-                if (++ws == SW) {
+                if (lane == 0) {
+                    mbar_arrive(&a_full[as]);
+                    mbar_arrive(&a_full[as + 1]);
+                }
+                if ((ws += 2) == SW) {
                     ws = 0;
                     wphase ^= 1u;
                 }
-                if (++as == ST) {
+                if ((as += 2) == ST) {
                     as = 0;
                     aphase ^= 1u;
                 }
