@@ -47,10 +47,11 @@ MAX_COPIES = 64            # cap for tiny inputs (the correctness-only configura
 LAUNCHES_PER_GRAPH = 50    # launches per captured CUDA graph (rounded to the copy cycle)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = {
-    "quantize_pack": ["w4a16_matmul_asym_b300/csrc/quantize_pack.cuh"],
-    "gemv": ["w4a16_matmul_asym_b300/csrc/gemv_dp4a.cuh", "w4a16_matmul_asym_b300/csrc/gemv.cuh"],
-    "gemm_tcgen05": ["w4a16_matmul_asym_b300/csrc/gemm_tcgen05.cuh"],
+KERNEL_SOURCES = {  # every file a kernel is compiled from (its digest dates a profile)
+    "quantize_pack": ["w4a16_matmul_asym_b300/csrc/quantize_pack.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
+    "gemv": ["w4a16_matmul_asym_b300/csrc/gemv_dp4a.cuh", "w4a16_matmul_asym_b300/csrc/gemv.cuh",
+             "w4a16_matmul_asym_b300/csrc/common.cuh"],
+    "gemm_tcgen05": ["w4a16_matmul_asym_b300/csrc/gemm_tcgen05.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
 }
 
 

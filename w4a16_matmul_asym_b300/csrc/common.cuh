@@ -99,6 +99,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Bounded wait for roles off the critical path (producer refills, epilogue): between
+// polls the thread backs off with __nanosleep (16 ns doubling to 256 ns), so it takes
+// few issue slots from the consumer warps sharing its SM sub-partition.
+__device__ __forceinline__ bool mbar_wait_polite(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                 unsigned long long timeout_ns) {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned int ns = 16;
+    for (;;) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+        if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            record_error(W4_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ---- bulk / tensor copies (TMA) ---------------------------------------------------
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.

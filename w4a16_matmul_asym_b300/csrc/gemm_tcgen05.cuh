@@ -62,6 +62,7 @@ constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int DEQ_WARP0 = 12;
 constexpr int NUM_DEQ_WARPS = 8;
+constexpr uint32_t BAR_EPI = 1;               // named barrier of the epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;            // accumulator region
 constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
@@ -280,6 +281,21 @@ __device__ __forceinline__ void produce(const CUtensorMap *map, uint8_t *ring, u
     }
 }
 
+// Named barrier over `threads` (whole warps) that also ORs one flag from every thread,
+// so that all participants take the same decision.
+__device__ __forceinline__ uint32_t named_bar_or(uint32_t id, uint32_t threads, uint32_t flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.or.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(threads), "r"(flag)
+        : "memory");
+    return r;
+}
+
 struct Params {
     const __half *scales;
     const uint8_t *zeros;
@@ -433,7 +449,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int mi = tile % m_tiles, ni = tile / m_tiles;
-            if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, tmo)) break;
+            // One warp polls the accumulator barrier; the others sleep on a named barrier
+            // and leave the issue slots to the dequantize warps.  The OR of the poller's
+            // result gives every warp the same decision.
+            uint32_t stop = 0;
+            if (warp == EPI_WARP0) stop = warp_wait(&acc_full[acc], acc_phase, abort_flag, tmo) ? 0u : 1u;
+            if (named_bar_or(BAR_EPI, NUM_EPI_WARPS * 32, stop)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    acc * 128u + static_cast<uint32_t>(half * cols);
