@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
             const int r0 = n_begin + lt * R;
             const int rows = min(R, n_end - r0);
             int got = 1;
-            if (lane == 0) got = mbar_wait_polite(&red_full[slot], sphase, abort_flag, tmo);
+            if (lane == 0) got = mbar_wait(&red_full[slot], sphase, abort_flag, tmo);
             got = __shfl_sync(0xffffffffu, got, 0);
             __syncwarp();
             if (!got) break;

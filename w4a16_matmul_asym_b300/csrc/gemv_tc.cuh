@@ -8,10 +8,12 @@
 //
 // Why tensor cores here: the prefill GEMM tiles W by 128 rows, so for a small N it
 // leaves most SMs idle.  This kernel splits K inside the MMA instead (below) and tiles
-// W by 8 or 16 rows.  One tcgen05.mma (M = 128, K = 16) costs about the same whatever
-// its N, so N carries all activation rows at once and the CUDA cores only unpack; the
-// MMA rate (and the lower clock the tensor cores run at) caps the kernel near 10
-// weights per SM clock, so it is used for 9 <= M <= 16 only.
+// W by 8 or 16 rows.  N carries all activation rows at once and the CUDA cores only
+// unpack.  With a tile of only 8 or 16 rows, each tile's MMAs are short (four units of
+// 64 levels for K = 4096) next to its fixed costs (the accumulator hand-off and an
+// epilogue that reads one column per activation row and sums the parts), so the kernel
+// runs well below both the MMA rate and HBM bandwidth; it is used for 9 <= M <= 16,
+// where it beats the CUDA-core kernels, and not for M <= 8, where it does not.
 //
 // Layout of the contraction.  A tile is R = 128 / P rows of W, each split into P
 // contiguous parts of KP = K / P levels; TMEM lane i holds row i / P, part i % P, so a
