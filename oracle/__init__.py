@@ -1,8 +1,8 @@
 """CPU oracle (test infrastructure only): see oracle.py and w4a16_oracle.c."""
 from .oracle import (GROUP, REL_TOL, bf16_bits_to_f64, bf16_to_f64, build, check_y,
-                     dequantize, f16_to_f32, f32_to_f16_bits, matmul, matmul_entries,
-                     quantize_pack, ulp_bf16, unpack, y_tolerance)
+                     dequantize, dequantize16, f16_to_f32, f32_to_bf16_bits, f32_to_f16_bits,
+                     matmul, matmul_entries, quantize_pack, ulp_bf16, unpack, y_tolerance)
 
 __all__ = ["GROUP", "REL_TOL", "bf16_bits_to_f64", "bf16_to_f64", "build", "check_y",
-           "dequantize", "f16_to_f32", "f32_to_f16_bits", "matmul", "matmul_entries",
-           "quantize_pack", "ulp_bf16", "unpack", "y_tolerance"]
+           "dequantize", "dequantize16", "f16_to_f32", "f32_to_bf16_bits", "f32_to_f16_bits",
+           "matmul", "matmul_entries", "quantize_pack", "ulp_bf16", "unpack", "y_tolerance"]

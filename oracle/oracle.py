@@ -61,6 +61,12 @@ def _load():
     i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
     lib.oracle_quantize_pack.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
     lib.oracle_quantize_pack.restype = ctypes.c_int
+    lib.oracle_quantize_pack_sym.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
+    lib.oracle_quantize_pack_sym.restype = ctypes.c_int
+    lib.oracle_dequantize_16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, vp]
+    lib.oracle_dequantize_16.restype = ctypes.c_int
+    lib.oracle_f32_to_bf16_bits.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16_bits.restype = ctypes.c_uint16
     lib.oracle_unpack.argtypes = [vp, i64, i64, vp]
     lib.oracle_unpack.restype = ctypes.c_int
     lib.oracle_dequantize.argtypes = [vp, vp, vp, i64, i64, dp]
@@ -92,11 +98,12 @@ def _as_u16_bits(x: np.ndarray) -> np.ndarray:
     raise TypeError(f"expected float16 or uint16 bit patterns, got {x.dtype}")
 
 
-def quantize_pack(W: np.ndarray, with_fp32_scales: bool = False):
+def quantize_pack(W: np.ndarray, with_fp32_scales: bool = False, symmetric: bool = False):
     """Quantize W[N,K] (float16 or float32) with groups of 128 along K.
 
     Returns (qweight uint8 [N,K/2], scales float16 [N,K/128], zeros uint8 [N,K/128])
-    and, if asked, the fp32 scales [N,K/128] used for q and zp.
+    and, if asked, the fp32 scales [N,K/128] used for q and zp.  symmetric=True takes
+    the absmax / 7 variant (levels q + 8, zero points 8).
     """
     if W.ndim != 2:
         raise ValueError("W must be 2-D [N,K]")
@@ -114,7 +121,8 @@ def quantize_pack(W: np.ndarray, with_fp32_scales: bool = False):
     s = np.empty((N, ng), np.uint16)
     z = np.empty((N, ng), np.uint8)
     s32 = np.empty((N, ng), np.float32)
-    rc = _load().oracle_quantize_pack(_ptr(src), dt, N, K, _ptr(q), _ptr(s), _ptr(z), _ptr(s32))
+    fn = _load().oracle_quantize_pack_sym if symmetric else _load().oracle_quantize_pack
+    rc = fn(_ptr(src), dt, N, K, _ptr(q), _ptr(s), _ptr(z), _ptr(s32))
     if rc:
         raise RuntimeError(f"oracle_quantize_pack failed ({rc})")
     out = (q, s.view(np.float16), z)
@@ -141,6 +149,30 @@ def dequantize(qweight, scales, zeros, K: int) -> np.ndarray:
     if _load().oracle_dequantize(_ptr(qweight), _ptr(s), _ptr(z), N, K, _ptr(out)):
         raise RuntimeError("oracle_dequantize failed")
     return out
+
+
+def dequantize16(qweight, scales, zeros, K: int, out_dtype: str = "bf16") -> np.ndarray:
+    """(q - zp) * fp16 scale rounded once to bfloat16 or float16, as uint16 bit
+    patterns [N,K]."""
+    if out_dtype not in ("bf16", "fp16"):
+        raise ValueError("out_dtype must be 'bf16' or 'fp16'")
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint8)
+    s = _as_u16_bits(scales)
+    z = np.ascontiguousarray(zeros, dtype=np.uint8)
+    N = qweight.shape[0]
+    out = np.empty((N, K), np.uint16)
+    rc = _load().oracle_dequantize_16(_ptr(qweight), _ptr(s), _ptr(z), N, K,
+                                      0 if out_dtype == "bf16" else 1, _ptr(out))
+    if rc:
+        raise RuntimeError(f"oracle_dequantize_16 failed ({rc})")
+    return out
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Element-wise binary32 -> bfloat16 bit patterns (round to nearest even)."""
+    lib = _load()
+    flat = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    return np.array([lib.oracle_f32_to_bf16_bits(float(v)) for v in flat], np.uint16).reshape(np.shape(x))
 
 
 def matmul(A_bf16: np.ndarray, qweight, scales, zeros):

@@ -28,12 +28,26 @@
  *   division; round half to even; scales stored as fp16, zero-points as uint8;
  *   dequantization uses the stored fp16 scale.
  *
+ *   - Symmetric variant: "Build a GPTQ INT4 Quantization Engine in Python/NumPy",
+ *     "Step 2" (per-group absmax, scale = absmax / 7 with 1 for an all-zero group,
+ *     q = clip(round(w / scale), -8, 7)); the group-wise INT4 layer page
+ *     ("Building a From-Scratch Group-Wise INT4 Quantization Layer for LLaMA
+ *     Weights", "Key design decisions") names symmetric per-group scales as the
+ *     standard choice for transformer weights.
+ *
  * Readings taken where the pages are silent or disagree (listed in the design doc):
  *   - q and zp are computed with the fp32 scale; only dequantization uses the
  *     stored fp16 scale.
  *   - q = clip(rint(w / s) + zp, 0, 15), i.e. rounding happens before adding zp
  *     (the pure-Python GPTQ page), not rint((w - min) / s).
  *   - Inputs are finite with a finite range; nothing here checks NaN/Inf.
+ *   - Symmetric: groups along K as for the asymmetric format (the NumPy page groups
+ *     output channels); the signed level q in [-8, 7] is stored as q + 8 with a zero
+ *     point of 8, so (level - 8) * scale is the page's q * scale and the asymmetric
+ *     layout and matmul apply unchanged.  The group-wise INT4 layer page's listing
+ *     (scale = absmax, quantizing |w|) loses the sign and is not followed.
+ *   - Dequantized output as a 16-bit tensor: the exact product (q - zp) * s16
+ *     rounded once to nearest-even bfloat16 or binary16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -95,6 +109,22 @@ uint16_t oracle_f32_to_f16_bits(float xf)
     return sign | (uint16_t)(ebits << 10) | fbits;
 }
 
+/* Round a binary32 value to the nearest bfloat16, ties to even.  bfloat16 keeps the
+ * sign, the 8 exponent bits and the top 7 fraction bits of binary32, so the result is
+ * the high 16 bits, plus one when the dropped low 16 bits are above half an ulp
+ * (0x8000), or exactly half with an odd kept pattern.  A carry out of the fraction
+ * moves to the next binade (or to Inf), which is the correctly rounded value. */
+uint16_t oracle_f32_to_bf16_bits(float xf)
+{
+    uint32_t u;
+    memcpy(&u, &xf, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu))
+        return (uint16_t)((u >> 16) | 0x0040u);   /* NaN stays a quiet NaN */
+    uint32_t hi = u >> 16, lo = u & 0xffffu;
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;
+    return (uint16_t)hi;
+}
+
 /* bfloat16 is the high half of a binary32 pattern: widening is a 16-bit shift. */
 double oracle_bf16_to_f64(uint16_t b)
 {
@@ -138,6 +168,27 @@ static void quantize_group(const float *w, int G, uint8_t *q, float *scale, int 
     *zero = zp;
 }
 
+/* ---- quantize one group, symmetric ------------------------------------------ */
+/* Page steps: absmax over the group, scale = absmax / 7 (IEEE fp32 division; 1 for
+ * an all-zero group), q = clip(round_half_even(w / scale), -8, 7).  Stored level =
+ * q + 8 with zero point 8. */
+static void quantize_group_sym(const float *w, int G, uint8_t *q, float *scale, int *zero)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < G; ++i) {
+        float a = fabsf(w[i]);
+        if (a > amax) amax = a;
+    }
+    float s = (amax == 0.0f) ? 1.0f : amax / 7.0f;
+    for (int i = 0; i < G; ++i) {
+        float t = rintf(w[i] / s);
+        float c = fminf(fmaxf(t, -8.0f), 7.0f);
+        q[i] = (uint8_t)((int)c + 8);
+    }
+    *scale = s;
+    *zero = 8;
+}
+
 /* Quantize and pack W[N,K] (row-major, K contiguous).
  *   w_dtype: 0 = fp16 bits (uint16), 1 = fp32
  *   qweight: uint8 [N, K/2], element 2j in the low nibble, 2j+1 in the high nibble
@@ -145,9 +196,8 @@ static void quantize_group(const float *w, int G, uint8_t *q, float *scale, int 
  *   zeros  : uint8 [N, K/128]
  *   scales32 (optional, may be NULL): the fp32 scales, for tests of the bound.
  * Returns 0, or -1 on invalid arguments. */
-int oracle_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K,
-                         uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
-                         float *scales32)
+static int quantize_pack_mode(const void *W, int w_dtype, int64_t N, int64_t K, int symmetric,
+                              uint8_t *qweight, uint16_t *scales, uint8_t *zeros, float *scales32)
 {
     if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
     if (w_dtype != 0 && w_dtype != 1) return -1;
@@ -165,7 +215,10 @@ int oracle_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K,
             }
             float s;
             int zp;
-            quantize_group(wbuf, ORACLE_GROUP, qbuf, &s, &zp);
+            if (symmetric)
+                quantize_group_sym(wbuf, ORACLE_GROUP, qbuf, &s, &zp);
+            else
+                quantize_group(wbuf, ORACLE_GROUP, qbuf, &s, &zp);
             scales[n * ng + g] = oracle_f32_to_f16_bits(s);
             zeros[n * ng + g] = (uint8_t)zp;
             if (scales32) scales32[n * ng + g] = s;
@@ -176,6 +229,21 @@ int oracle_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K,
         }
     }
     return 0;
+}
+
+int oracle_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K,
+                         uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
+                         float *scales32)
+{
+    return quantize_pack_mode(W, w_dtype, N, K, 0, qweight, scales, zeros, scales32);
+}
+
+/* The symmetric variant: same layouts, zero points all 8. */
+int oracle_quantize_pack_sym(const void *W, int w_dtype, int64_t N, int64_t K,
+                             uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
+                             float *scales32)
+{
+    return quantize_pack_mode(W, w_dtype, N, K, 1, qweight, scales, zeros, scales32);
 }
 
 /* Unpack qweight[N,K/2] into q[N,K] (one value 0..15 per byte). */
@@ -215,6 +283,36 @@ int oracle_dequantize(const uint8_t *qweight, const uint16_t *scales, const uint
 {
     if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
     dequant_rows(qweight, scales, zeros, 0, N, K, W_hat);
+    return 0;
+}
+
+/* Dequantize into a 16-bit tensor: out[n,k] = RNE((q - zp) * s16), out_dtype 0 =
+ * bfloat16, 1 = binary16 (bit patterns).  The fp64 product is exact and also exact in
+ * binary32 (a 5-bit integer times an 11-bit significand), so it is narrowed to
+ * binary32 without rounding and then rounded once. */
+int oracle_dequantize_16(const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                         int64_t N, int64_t K, int out_dtype, uint16_t *out)
+{
+    if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    if (out_dtype != 0 && out_dtype != 1) return -1;
+    double row[ORACLE_GROUP];
+    const int64_t ng = K / ORACLE_GROUP;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < ng; ++g) {
+            for (int i = 0; i < ORACLE_GROUP; ++i) {
+                int64_t k = g * ORACLE_GROUP + i;
+                uint8_t b = qweight[n * (K / 2) + k / 2];
+                int q = (k & 1) ? (b >> 4) & 0x0f : b & 0x0f;
+                double s = (double)oracle_f16_to_f32(scales[n * ng + g]);
+                row[i] = (double)(q - zeros[n * ng + g]) * s;
+            }
+            for (int i = 0; i < ORACLE_GROUP; ++i) {
+                float f = (float)row[i];
+                if ((double)f != row[i]) return -2;   /* cannot happen; see above */
+                out[n * K + g * ORACLE_GROUP + i] =
+                    out_dtype == 0 ? oracle_f32_to_bf16_bits(f) : oracle_f32_to_f16_bits(f);
+            }
+        }
     return 0;
 }
 

@@ -278,3 +278,109 @@ def test_tolerance_closed_forms(oracle_mod):
     # a nonzero output where the reference is exactly 0 with S = 0 fails
     ok, _, _ = oracle_mod.check_y(np.array([0x3F80, 0xC040, 0x0001], np.uint16), Yref, S)
     assert not ok
+
+
+# ---- symmetric variant and 16-bit dequantize ----------------------------------------
+SYM_CASES = parse_cases(os.path.join(GOLDEN_DIR, "sym_groups.txt"))
+
+
+@pytest.mark.parametrize("case", SYM_CASES, ids=[c["name"] for c in SYM_CASES])
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_symmetric_hand_worked_groups(oracle_mod, case, dtype):
+    """Hand-worked symmetric groups (tests/golden/sym_groups.txt), placed second in a
+    row of three groups."""
+    g, nv = _group_from_case(case)
+    if dtype == "f16":
+        assert case["f16_exact"] == "1"
+        assert np.array_equal(g.astype(np.float16).astype(np.float32), g)
+        W = g.astype(np.float16)[None, :]
+    else:
+        W = g[None, :]
+    rng = np.random.default_rng(8)
+    row = rng.standard_normal(384).astype(W.dtype)
+    row[128:256] = W[0]
+    q, s16, z, s32 = oracle_mod.quantize_pack(row[None, :], with_fp32_scales=True, symmetric=True)
+    assert s32[0, 1].view(np.uint32) == int(case["scale_f32"], 16)
+    assert s16[0, 1].view(np.uint16) == int(case["scale_f16"], 16)
+    assert np.all(z == 8)
+    qq = oracle_mod.unpack(q, 384)[0, 128:256]
+    assert list(qq[:nv]) == [int(x) for x in case["q"].split()]
+    assert np.all(qq[nv:] == int(case["q_pad"]))
+
+
+def test_symmetric_odd_symmetry(oracle_mod):
+    """Negating W mirrors every level about the zero point (level -> 16 - level) and
+    keeps the scales: round-half-even and the clip are odd functions.  A dropped sign,
+    a round-half-up or an offset other than 8 breaks it."""
+    rng = np.random.default_rng(11)
+    for dt in (np.float16, np.float32):
+        W = (rng.standard_normal((8, 512)) * 0.02).astype(dt)
+        W[rng.random(W.shape) < 0.01] *= 10
+        q1, s1, z1 = oracle_mod.quantize_pack(W, symmetric=True)
+        q2, s2, z2 = oracle_mod.quantize_pack(-W, symmetric=True)
+        l1 = oracle_mod.unpack(q1, 512).astype(int)
+        l2 = oracle_mod.unpack(q2, 512).astype(int)
+        assert np.array_equal(s1.view(np.uint16), s2.view(np.uint16))
+        assert np.array_equal(l2, 16 - l1)
+        assert np.all(z1 == 8) and np.all(z2 == 8)
+
+
+def test_symmetric_bounds(oracle_mod):
+    """Levels in [1, 15]; each element within half a step (fp32 scale) of (level - 8) *
+    scale, up to the fp32 quotient's rounding; the largest |w| of a group maps to level
+    1 or 15 (q = -7 or 7)."""
+    rng = np.random.default_rng(12)
+    W = (rng.standard_normal((16, 1024)) * 0.02).astype(np.float32)
+    W[rng.random(W.shape) < 0.001] *= 10
+    q, s16, z, s32 = oracle_mod.quantize_pack(W, with_fp32_scales=True, symmetric=True)
+    lv = oracle_mod.unpack(q, 1024).astype(np.float64)
+    assert lv.min() >= 1 and lv.max() <= 15
+    s = np.repeat(s32.astype(np.float64), 128, axis=1)
+    err = np.abs(W.astype(np.float64) - (lv - 8) * s)
+    assert np.all(err <= s * (0.5 + 2.0 ** -20))
+    g = np.abs(W).reshape(16, 8, 128)
+    top = np.take_along_axis(lv.reshape(16, 8, 128), g.argmax(axis=2)[..., None], axis=2)
+    assert np.all((top == 1) | (top == 15))
+
+
+def test_bf16_rounding_against_torch(oracle_mod):
+    """binary32 -> bfloat16 rounding against torch's CPU conversion (round to nearest
+    even): random magnitudes over the whole exponent range, exact ties, values that
+    carry into the next binade, zeros, subnormals and overflow to infinity."""
+    import torch
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(4000) * 10.0 ** rng.integers(-37, 37, 4000)).astype(np.float32)
+    ties = (rng.standard_normal(1000).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)) | np.uint32(0x8000)
+    carry = np.array([0x3F7FFFFF, 0x3FFFFFFF, 0x7F7FFFFF, 0x7F7F8000, 0x00008000, 0x00018000,
+                      0x00000001, 0x807FFFFF, 0x80000000, 0x00000000, 0x3F808000, 0x3F818000],
+                     np.uint32)
+    x = np.concatenate([x, ties.view(np.float32), carry.view(np.float32)])
+    ours = oracle_mod.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+@pytest.mark.parametrize("out", ["bf16", "fp16"])
+def test_dequantize16_is_the_exact_product_rounded_once(oracle_mod, out):
+    """The 16-bit dequantize equals the fp64 dequantize (pinned above) rounded by a
+    library: numpy's float64 -> float16 and torch's float64 -> bfloat16 conversions
+    (round to nearest even).  Scales span subnormal to large fp16 values, so fp16
+    outputs include subnormals and overflow to infinity."""
+    import torch
+    rng = np.random.default_rng(9)
+    N, K = 16, 512
+    q = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    mag = 10.0 ** rng.integers(-7, 4, (N, K // 128))
+    s = (rng.standard_normal((N, K // 128)) * mag).astype(np.float16)
+    s[0, 0] = np.float16(8000.0)          # 15 * 8000 overflows fp16
+    z = rng.integers(0, 16, (N, K // 128), dtype=np.uint8)
+    z[0, 0] = 0
+    exact = oracle_mod.dequantize(q, s, z, K)
+    got = oracle_mod.dequantize16(q, s, z, K, out)
+    if out == "fp16":
+        with np.errstate(over="ignore"):
+            ref = exact.astype(np.float16).view(np.uint16)
+        assert np.isinf(got.view(np.float16)).any()
+    else:
+        ref = torch.from_numpy(exact).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
