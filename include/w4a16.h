@@ -48,8 +48,9 @@ typedef enum {
     W4_ERR_TIMEOUT = 5        /* a kernel gave up a bounded wait (see w4_check_device_error) */
 } w4_status;
 
-/* Element type of W for w4_quantize_pack. */
-typedef enum { W4_DTYPE_F16 = 0, W4_DTYPE_F32 = 1 } w4_dtype;
+/* Element types: of W for w4_quantize_pack / w4_quantize_pack_sym (F16, F32), of the
+ * output of w4_dequantize (F16, BF16). */
+typedef enum { W4_DTYPE_F16 = 0, W4_DTYPE_F32 = 1, W4_DTYPE_BF16 = 2 } w4_dtype;
 
 #define W4_GROUP_SIZE 128
 
@@ -84,6 +85,50 @@ typedef enum { W4_DTYPE_F16 = 0, W4_DTYPE_F32 = 1 } w4_dtype;
  */
 W4_API int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, int group,
                      uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream);
+
+/*
+ * w4_quantize_pack_sym -- the symmetric variant of w4_quantize_pack: per group of 128
+ * elements along K, with values widened exactly to fp32,
+ *     s  = (absmax == 0) ? 1 : absmax / 7                 (fp32, IEEE division;
+ *                                                           absmax = max |w| of the group)
+ *     q  = clip(round_half_even(w / s), -8, 7)            (IEEE fp32 division by s)
+ *     scales = fp16_round_nearest_even(s), zeros = 8, stored level = q + 8,
+ * i.e. the layout of w4_quantize_pack with every zero point 8, so that w4_matmul and
+ * w4_dequantize consume it unchanged ((level - 8) * s = q * s).  Since |w / s| <= 7 up
+ * to the rounding of the quotient, the stored levels lie in [1, 15].
+ *
+ * Defined by: "Build a GPTQ INT4 Quantization Engine in Python/NumPy" (Step 2: per-group
+ * absmax, scale = absmax / 7 with 1 for an all-zero group, q = clip(round(w / scale),
+ * -8, 7)); "Building a From-Scratch Group-Wise INT4 Quantization Layer for LLaMA
+ * Weights" (Key design decisions: symmetric per-group scales as the standard choice for
+ * transformer weights).  Bit-exact with the definition above for finite inputs.
+ *
+ * Arguments, alignment, empty problems and errors: as w4_quantize_pack.
+ */
+W4_API int w4_quantize_pack_sym(const void *W, int w_dtype, int64_t N, int64_t K, int group,
+                                uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream);
+
+/*
+ * w4_dequantize -- materialize W_hat[N,K] = (q - zp) * scale_fp16 as a 16-bit tensor,
+ * the explicit dequantize path for a consumer that wants the whole weight matrix.
+ *
+ * Defined by: "From Scratch: Building a GPTQ INT4 Quantizer in Pure Python" (Step 4:
+ * dequantize = (q - zero_point) * scale).  Exact convention: the product (q - zp) * s16
+ * is exact in fp32 and is rounded once to nearest-even bf16 (out_dtype W4_DTYPE_BF16)
+ * or fp16 (W4_DTYPE_F16; a magnitude past the fp16 range gives +-inf).  Bit-exact.
+ *
+ * Arguments:
+ *   qweight, scales, zeros  as written by w4_quantize_pack or w4_quantize_pack_sym
+ *            (same alignment rules).
+ *   N, K     N >= 0, K >= 0, K % group == 0.
+ *   group    must be 128.
+ *   out_dtype W4_DTYPE_BF16 or W4_DTYPE_F16 (others: W4_ERR_INVALID_ARG).
+ *   out      device pointer, 16-bit [N, K]; 16-byte aligned.  Written.
+ *   stream   the stream to run on.
+ * N == 0 or K == 0: W4_OK, nothing launched.
+ */
+W4_API int w4_dequantize(const uint8_t *qweight, const void *scales, const uint8_t *zeros, int64_t N,
+                         int64_t K, int group, int out_dtype, void *out, cudaStream_t stream);
 
 /*
  * w4_matmul -- Y[M,N] = A[M,K] * W_hat[N,K]^T with W_hat = (q - zp) * scale_fp16,

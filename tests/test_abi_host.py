@@ -103,6 +103,52 @@ def test_matmul_null_and_misaligned(lib):
     assert lib.w4_matmul(FAKE, 2, 4, 256, 128, FAKE, FAKE, FAKE, FAKE + 1, None) == 3
 
 
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, 0, -1, 128, 128), 1),
+    ((FAKE, 0, 4, 130, 128), 1),
+    ((FAKE, 0, 4, 128, 64), 2),
+    ((FAKE, 7, 4, 128, 128), 1),
+    ((0, 0, 4, 128, 128), 1),
+    ((FAKE + 8, 1, 4, 128, 128), 3),
+    ((FAKE, 0, 0, 128, 128), 0),
+    ((FAKE, 1, 4, 0, 128), 0),
+])
+def test_quantize_pack_sym_validation(lib, args, expect):
+    """The symmetric quantizer validates exactly as w4_quantize_pack."""
+    W, dt, N, K, G = args
+    assert lib.w4_quantize_pack_sym(W, dt, N, K, G, FAKE, FAKE, FAKE, None) == expect
+    assert lib.w4_quantize_pack_sym(FAKE, 0, 4, 128, 128, FAKE + 4, FAKE, FAKE, None) == 3
+    assert lib.w4_quantize_pack_sym(FAKE, 0, 4, 128, 128, FAKE, FAKE, 0, None) == 1
+
+
+BF16, F16, F32 = 2, 0, 1
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((-1, 256, 128, BF16), 1),           # negative N
+    ((4, -256, 128, BF16), 1),           # negative K
+    ((4, 100, 128, BF16), 1),            # K not a multiple of the group
+    ((4, 256, 64, BF16), 2),             # group 64 unsupported
+    ((4, 256, 128, F32), 1),             # fp32 output is not offered
+    ((4, 256, 128, 9), 1),               # unknown dtype
+    ((0, 256, 128, F16), 0),             # empty
+    ((4, 0, 128, BF16), 0),              # empty
+])
+def test_dequantize_validation(lib, args, expect):
+    N, K, G, dt = args
+    assert lib.w4_dequantize(FAKE, FAKE, FAKE, N, K, G, dt, FAKE, None) == expect
+
+
+def test_dequantize_null_and_misaligned(lib):
+    assert lib.w4_dequantize(0, FAKE, FAKE, 4, 256, 128, BF16, FAKE, None) == 1
+    assert lib.w4_dequantize(FAKE, 0, FAKE, 4, 256, 128, BF16, FAKE, None) == 1
+    assert lib.w4_dequantize(FAKE, FAKE, 0, 4, 256, 128, BF16, FAKE, None) == 1
+    assert lib.w4_dequantize(FAKE, FAKE, FAKE, 4, 256, 128, BF16, 0, None) == 1
+    assert lib.w4_dequantize(FAKE + 4, FAKE, FAKE, 4, 256, 128, BF16, FAKE, None) == 3
+    assert lib.w4_dequantize(FAKE, FAKE + 1, FAKE, 4, 256, 128, BF16, FAKE, None) == 3
+    assert lib.w4_dequantize(FAKE, FAKE, FAKE, 4, 256, 128, F16, FAKE + 8, None) == 3
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from w4a16_matmul_asym_b300 import _binding
     with pytest.raises(ImportError):

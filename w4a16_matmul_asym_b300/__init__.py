@@ -3,15 +3,16 @@
 The compute lives in libw4a16.so (hand-written CUDA for sm_103a behind a C ABI,
 declared in include/w4a16.h).  This package is its thin Python binding.
 """
-from ._binding import (EXPORTED, GROUP_SIZE, LIB_PATH, W4_DTYPE_F16, W4_DTYPE_F32,
+from ._binding import (EXPORTED, GROUP_SIZE, LIB_PATH, W4_DTYPE_BF16, W4_DTYPE_F16, W4_DTYPE_F32,
                        W4_ERR_CUDA, W4_ERR_INVALID_ARG, W4_ERR_MISALIGNED, W4_ERR_TIMEOUT,
-                       W4_ERR_UNSUPPORTED, W4_OK, W4Error, load_library, matmul,
+                       W4_ERR_UNSUPPORTED, W4_OK, W4Error, dequantize, load_library, matmul,
                        quantize_pack, status_string, w4_check_device_error,
-                       w4_debug_inject_stall, w4_matmul, w4_quantize_pack,
-                       w4_set_wait_timeout_ns)
+                       w4_debug_inject_stall, w4_dequantize, w4_matmul, w4_quantize_pack,
+                       w4_quantize_pack_sym, w4_set_wait_timeout_ns)
 
-__all__ = ["EXPORTED", "GROUP_SIZE", "LIB_PATH", "W4_DTYPE_F16", "W4_DTYPE_F32",
+__all__ = ["EXPORTED", "GROUP_SIZE", "LIB_PATH", "W4_DTYPE_BF16", "W4_DTYPE_F16", "W4_DTYPE_F32",
            "W4_ERR_CUDA", "W4_ERR_INVALID_ARG", "W4_ERR_MISALIGNED", "W4_ERR_TIMEOUT",
-           "W4_ERR_UNSUPPORTED", "W4_OK", "W4Error", "load_library", "matmul",
+           "W4_ERR_UNSUPPORTED", "W4_OK", "W4Error", "dequantize", "load_library", "matmul",
            "quantize_pack", "status_string", "w4_check_device_error", "w4_debug_inject_stall",
-           "w4_matmul", "w4_quantize_pack", "w4_set_wait_timeout_ns"]
+           "w4_dequantize", "w4_matmul", "w4_quantize_pack", "w4_quantize_pack_sym",
+           "w4_set_wait_timeout_ns"]

@@ -21,11 +21,13 @@ W4_ERR_CUDA = 4
 W4_ERR_TIMEOUT = 5
 W4_DTYPE_F16 = 0
 W4_DTYPE_F32 = 1
+W4_DTYPE_BF16 = 2
 GROUP_SIZE = 128
 
 # Symbols declared in include/w4a16.h (checked by the host-side tests).
-EXPORTED = ("w4_quantize_pack", "w4_matmul", "w4_status_string", "w4_check_device_error",
-            "w4_set_wait_timeout_ns", "w4_debug_inject_stall")
+EXPORTED = ("w4_quantize_pack", "w4_quantize_pack_sym", "w4_dequantize", "w4_matmul",
+            "w4_status_string", "w4_check_device_error", "w4_set_wait_timeout_ns",
+            "w4_debug_inject_stall")
 
 
 class W4Error(RuntimeError):
@@ -49,6 +51,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.w4_quantize_pack.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp, vp, vp]
     lib.w4_quantize_pack.restype = ctypes.c_int
+    lib.w4_quantize_pack_sym.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+    lib.w4_quantize_pack_sym.restype = ctypes.c_int
+    lib.w4_dequantize.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]
+    lib.w4_dequantize.restype = ctypes.c_int
     lib.w4_matmul.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp]
     lib.w4_matmul.restype = ctypes.c_int
     lib.w4_status_string.argtypes = [ctypes.c_int]
@@ -72,6 +78,18 @@ def w4_quantize_pack(W_ptr: int, w_dtype: int, N: int, K: int, group: int,
                      qweight_ptr: int, scales_ptr: int, zeros_ptr: int, stream: int) -> int:
     return load_library().w4_quantize_pack(W_ptr, w_dtype, N, K, group, qweight_ptr,
                                            scales_ptr, zeros_ptr, stream)
+
+
+def w4_quantize_pack_sym(W_ptr: int, w_dtype: int, N: int, K: int, group: int,
+                         qweight_ptr: int, scales_ptr: int, zeros_ptr: int, stream: int) -> int:
+    return load_library().w4_quantize_pack_sym(W_ptr, w_dtype, N, K, group, qweight_ptr,
+                                               scales_ptr, zeros_ptr, stream)
+
+
+def w4_dequantize(qweight_ptr: int, scales_ptr: int, zeros_ptr: int, N: int, K: int, group: int,
+                  out_dtype: int, out_ptr: int, stream: int) -> int:
+    return load_library().w4_dequantize(qweight_ptr, scales_ptr, zeros_ptr, N, K, group, out_dtype,
+                                        out_ptr, stream)
 
 
 def w4_matmul(A_ptr: int, M: int, N: int, K: int, group: int, qweight_ptr: int,
@@ -100,11 +118,12 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream)
 
 
-def quantize_pack(W, group: int = GROUP_SIZE, stream=None, out=None):
+def quantize_pack(W, group: int = GROUP_SIZE, stream=None, out=None, symmetric: bool = False):
     """Quantize a CUDA tensor W[N,K] (float16 or float32).
 
     Returns (qweight uint8 [N,K/2], scales float16 [N,K/128], zeros uint8 [N,K/128]),
-    allocated with torch on W's device unless `out` supplies them.
+    allocated with torch on W's device unless `out` supplies them.  symmetric=True runs
+    w4_quantize_pack_sym (scale absmax / 7, zero points 8).
     """
     import torch
     if W.dim() != 2 or not W.is_cuda:
@@ -124,11 +143,38 @@ def quantize_pack(W, group: int = GROUP_SIZE, stream=None, out=None):
         zeros = torch.empty((N, ng), dtype=torch.uint8, device=W.device)
     else:
         qweight, scales, zeros = out
-    rc = w4_quantize_pack(W.data_ptr(), dt, N, K, group, qweight.data_ptr(),
-                          scales.data_ptr(), zeros.data_ptr(), _stream_handle(stream))
+    fn, name = (w4_quantize_pack_sym, "w4_quantize_pack_sym") if symmetric else (w4_quantize_pack, "w4_quantize_pack")
+    rc = fn(W.data_ptr(), dt, N, K, group, qweight.data_ptr(), scales.data_ptr(), zeros.data_ptr(),
+            _stream_handle(stream))
     if rc != W4_OK:
-        raise W4Error(rc, "w4_quantize_pack")
+        raise W4Error(rc, name)
     return qweight, scales, zeros
+
+
+def dequantize(qweight, scales, zeros, dtype=None, group: int = GROUP_SIZE, stream=None, out=None):
+    """W_hat[N,K] = (q - zp) * scale as a bfloat16 (default) or float16 CUDA tensor."""
+    import torch
+    dtype = torch.bfloat16 if dtype is None else dtype
+    if dtype == torch.bfloat16:
+        odt = W4_DTYPE_BF16
+    elif dtype == torch.float16:
+        odt = W4_DTYPE_F16
+    else:
+        raise TypeError("dtype must be torch.bfloat16 or torch.float16")
+    if qweight.dim() != 2 or not qweight.is_cuda or qweight.dtype != torch.uint8:
+        raise ValueError("qweight must be a 2-D uint8 CUDA tensor")
+    if scales.dtype != torch.float16 or zeros.dtype != torch.uint8:
+        raise TypeError("scales must be float16 and zeros uint8")
+    N, K = qweight.shape[0], qweight.shape[1] * 2
+    if out is None:
+        out = torch.empty((N, K), dtype=dtype, device=qweight.device)
+    elif out.dtype != dtype or tuple(out.shape) != (N, K) or not out.is_contiguous() or out.device != qweight.device:
+        raise ValueError(f"out must be a contiguous {dtype} tensor of shape ({N}, {K}) on {qweight.device}")
+    rc = w4_dequantize(qweight.data_ptr(), scales.data_ptr(), zeros.data_ptr(), N, K, group, odt,
+                       out.data_ptr(), _stream_handle(stream))
+    if rc != W4_OK:
+        raise W4Error(rc, "w4_dequantize")
+    return out
 
 
 def matmul(A, qweight, scales, zeros, group: int = GROUP_SIZE, stream=None, out=None):

@@ -8,6 +8,10 @@
 //   zp = clip(rhe(-min / s), 0, 15)
 //   q  = clip(rhe(w / s) + zp, 0, 15)                 IEEE fp32 quotient
 //   qweight byte j of a group = q[2j] | q[2j+1] << 4; scale stored as rne fp16(s).
+// Symmetric variant ("Build a GPTQ INT4 Quantization Engine in Python/NumPy", Step 2):
+//   s  = (absmax == 0) ? 1 : absmax / 7, absmax = max(|min|, |max|)   IEEE division
+//   zp = 8, so q = clip(rhe(w / s) + 8, 0, 15) = clip(rhe(w / s), -8, 7) + 8
+// and everything after the group parameters is shared.
 //
 // Layout: the flat group index G = n * (K/128) + g addresses every output directly:
 // qweight bytes [64 G, 64 G + 64), scales[G], zeros[G], and W elements
@@ -102,13 +106,20 @@ struct GroupParams {
     float zp;       // zero point (0..15) as float
 };
 
+template <bool kSym>
 __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
     GroupParams p;
-    p.s = (mx == mn) ? 1.0f : __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-    const float x = __fdiv_rn(-mn, p.s);
-    // rhe(x) for |x| < 2^22 via the magic add; larger |x| clips anyway.
-    const float zq = (fabsf(x) < 4194304.0f) ? __fsub_rn(__fadd_rn(x, kRoundMagic), kRoundMagic) : x;
-    p.zp = fminf(fmaxf(zq, 0.0f), 15.0f);
+    if constexpr (kSym) {
+        const float amax = fmaxf(fabsf(mn), fabsf(mx));   // exact
+        p.s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 7.0f);
+        p.zp = 8.0f;
+    } else {
+        p.s = (mx == mn) ? 1.0f : __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+        const float x = __fdiv_rn(-mn, p.s);
+        // rhe(x) for |x| < 2^22 via the magic add; larger |x| clips anyway.
+        const float zq = (fabsf(x) < 4194304.0f) ? __fsub_rn(__fadd_rn(x, kRoundMagic), kRoundMagic) : x;
+        p.zp = fminf(fmaxf(zq, 0.0f), 15.0f);
+    }
     const float rcp = __frcp_rn(p.s);
     const float mz = __fadd_rn(kRoundMagic, p.zp);
     p.rcp2 = f2pack(rcp, rcp);
@@ -185,7 +196,7 @@ struct QuantCfg {
 
 // One lane's 128 bytes of W (cur, natural order) -> its qweight words; the group's
 // scale and zero point are written by the lane with part 0.  g = flat group index.
-template <bool kF32>
+template <bool kF32, bool kSym>
 __device__ __forceinline__ void quantize_lane(const uint4 (&cur)[QuantCfg<kF32>::kLoads], int64_t g,
                                               int part, int64_t total_groups, uint32_t *__restrict__ qw,
                                               __half *__restrict__ scales, uint8_t *__restrict__ zeros) {
@@ -224,7 +235,7 @@ __device__ __forceinline__ void quantize_lane(const uint4 (&cur)[QuantCfg<kF32>:
         mn = widen_lo(pkb);
         mx = -widen_hi(pkb);
     }
-    const GroupParams p = group_params(mn, mx);
+    const GroupParams p = group_params<kSym>(mn, mx);
 
     // ---- quantize and pack, 8 elements per output word ----
     uint32_t words[C::kWords];
@@ -270,7 +281,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 1024;
 // W viewed as bytes in 128-byte lines: tmW is a 2-D map {128 B, total_lines} with
 // 128-byte swizzle.  Stage unit u covers lines [u * LINES, (u + 1) * LINES), i.e.
 // groups [u * CW * kGroupsPerWarp, ...); CTA b takes units b, b + gridDim.x, ...
-template <bool kF32>
+template <bool kF32, bool kSym>
 __global__ void __launch_bounds__(quant::NUM_THREADS, 1)
     quantize_pack_kernel(const __grid_constant__ CUtensorMap tmW, int64_t total_groups,
                          uint32_t *__restrict__ qw, __half *__restrict__ scales,
@@ -365,7 +376,7 @@ __global__ void __launch_bounds__(quant::NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             const int64_t g = ((blockIdx.x + lt * gridDim.x) * LINES) / kLinesPerGroup + warp * C::kGroupsPerWarp + gsub;
-            quantize_lane<kF32>(cur, g, part, total_groups, qw, scales, zeros);
+            quantize_lane<kF32, kSym>(cur, g, part, total_groups, qw, scales, zeros);
         }
     }
     __syncthreads();

@@ -10,6 +10,7 @@
 #include <utility>
 
 #include "common.cuh"
+#include "dequantize.cuh"
 #include "gemm_tcgen05.cuh"
 #include "gemv.cuh"
 #include "gemv_dp4a.cuh"
@@ -285,24 +286,10 @@ int launch_gemv(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const u
     }
 }
 
-}  // namespace
-
-extern "C" {
-
-const char *w4_status_string(int status) {
-    switch (status) {
-        case W4_OK: return "W4_OK";
-        case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG: invalid argument";
-        case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED: unsupported configuration (group must be 128)";
-        case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED: pointer alignment violated";
-        case W4_ERR_CUDA: return "W4_ERR_CUDA: CUDA call or kernel launch failed";
-        case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a kernel gave up a bounded wait";
-        default: return "unknown w4a16 status";
-    }
-}
-
-int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, int group,
-                     uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream) {
+// Both quantizers: validation, the tensor map of W and the launch.
+template <bool kSym>
+int quantize_pack_impl(const void *W, int w_dtype, int64_t N, int64_t K, int group, uint8_t *qweight,
+                       void *scales, uint8_t *zeros, cudaStream_t stream) {
     if (N < 0 || K < 0 || group <= 0) return W4_ERR_INVALID_ARG;
     if (w_dtype != W4_DTYPE_F16 && w_dtype != W4_DTYPE_F32) return W4_ERR_INVALID_ARG;
     if (group != W4_GROUP_SIZE) return W4_ERR_UNSUPPORTED;
@@ -330,13 +317,67 @@ int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, int group
     const dim3 block(w4::quant::NUM_THREADS);
     const w4::WaitParams wp = wait_params();
     if (w_dtype == W4_DTYPE_F16) {
-        auto kern = w4::quantize_pack_kernel<false>;
+        auto kern = w4::quantize_pack_kernel<false, kSym>;
         if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
         return launch(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
     }
-    auto kern = w4::quantize_pack_kernel<true>;
+    auto kern = w4::quantize_pack_kernel<true, kSym>;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
     return launch(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *w4_status_string(int status) {
+    switch (status) {
+        case W4_OK: return "W4_OK";
+        case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG: invalid argument";
+        case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED: unsupported configuration (group must be 128)";
+        case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED: pointer alignment violated";
+        case W4_ERR_CUDA: return "W4_ERR_CUDA: CUDA call or kernel launch failed";
+        case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        default: return "unknown w4a16 status";
+    }
+}
+
+int w4_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K, int group,
+                     uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream) {
+    return quantize_pack_impl<false>(W, w_dtype, N, K, group, qweight, scales, zeros, stream);
+}
+
+int w4_quantize_pack_sym(const void *W, int w_dtype, int64_t N, int64_t K, int group,
+                         uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream) {
+    return quantize_pack_impl<true>(W, w_dtype, N, K, group, qweight, scales, zeros, stream);
+}
+
+int w4_dequantize(const uint8_t *qweight, const void *scales, const uint8_t *zeros, int64_t N, int64_t K,
+                  int group, int out_dtype, void *out, cudaStream_t stream) {
+    if (N < 0 || K < 0 || group <= 0) return W4_ERR_INVALID_ARG;
+    if (out_dtype != W4_DTYPE_BF16 && out_dtype != W4_DTYPE_F16) return W4_ERR_INVALID_ARG;
+    if (group != W4_GROUP_SIZE) return W4_ERR_UNSUPPORTED;
+    if (K % group != 0) return W4_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return W4_OK;
+    if (!qweight || !scales || !zeros || !out) return W4_ERR_INVALID_ARG;
+    if (!aligned(qweight, 16) || !aligned(scales, 2) || !aligned(out, 16)) return W4_ERR_MISALIGNED;
+    if (N > INT64_MAX / K) return W4_ERR_INVALID_ARG;
+    int sms = 0;
+    if (int rc = current_sm_count(&sms)) return rc;
+    namespace dq = w4::deq;
+    const int64_t chunks = N * K / 8;                  // 8 levels per chunk
+    const int64_t per_block = static_cast<int64_t>(dq::NUM_THREADS) * dq::UNROLL;
+    int64_t blocks = (chunks + per_block - 1) / per_block;
+    const int64_t cap = static_cast<int64_t>(sms) * dq::BLOCKS_PER_SM;
+    if (blocks > cap) blocks = cap;
+    const uint32_t *qw = reinterpret_cast<const uint32_t *>(qweight);
+    const __half *sc = static_cast<const __half *>(scales);
+    uint4 *o = static_cast<uint4 *>(out);
+    if (out_dtype == W4_DTYPE_BF16)
+        return launch(dq::dequantize_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(dq::NUM_THREADS), 0,
+                      stream, qw, sc, zeros, o, chunks);
+    return launch(dq::dequantize_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(dq::NUM_THREADS), 0,
+                  stream, qw, sc, zeros, o, chunks);
 }
 
 int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const uint8_t *qweight,
