@@ -52,6 +52,7 @@ KERNEL_SOURCES = {  # every file a kernel is compiled from (its digest dates a p
     "gemv": ["w4a16_matmul_asym_b300/csrc/gemv_dp4a.cuh", "w4a16_matmul_asym_b300/csrc/gemv.cuh",
              "w4a16_matmul_asym_b300/csrc/common.cuh"],
     "gemm_tcgen05": ["w4a16_matmul_asym_b300/csrc/gemm_tcgen05.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
+    "dequantize": ["w4a16_matmul_asym_b300/csrc/dequantize.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
 }
 
 
@@ -370,6 +371,53 @@ def run_ours(args, ws, rank, local, dist):
                 "frac": ach / peak, "peak_source": peak_src,
                 "traffic": profiled_traffic(dom, args.workload)}
 
+    # The two further kernels (not part of the step): the symmetric quantizer on the
+    # same W copies, and the explicit dequantize of the packed copies into rotating
+    # bf16 outputs; same method (CUDA graphs of back-to-back launches, events around
+    # `steps` launches per kernel, inputs and outputs rotated over >= 3x L2).
+    if not args.no_extra:
+        out_bytes = N * K * 2
+        co = min(MAX_COPIES, max(2, -(-ROTATE_L2 * l2 // out_bytes)))
+        outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(co)]
+
+        def time_phase(launch_i, period):
+            n = period * max(1, -(-LAUNCHES_PER_GRAPH // period))
+            reps, rest = divmod(steps, n)
+
+            def graph_of(count):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    for i in range(count):
+                        launch_i(i, cap)
+                return g
+            g_full = graph_of(n)
+            g_rest = graph_of(rest) if rest else None
+            g_full.replay()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g_full.replay()
+            if g_rest is not None:
+                g_rest.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / 1e3 / steps
+
+        sym_s = time_phase(lambda i, s_: w4.quantize_pack(Wds[i % cw], out=(qs[i % cm], ss[i % cm], zs[i % cm]),
+                                                          stream=s_, symmetric=True), R)
+        dq_period = cm * co // math.gcd(cm, co)
+        dq_s = time_phase(lambda i, s_: w4.dequantize(qs[i % cm], ss[i % cm], zs[i % cm], dtype=torch.bfloat16,
+                                                      out=outs[i % co], stream=s_), dq_period)
+        dqb = qsz_bytes + out_bytes
+        kernels["quantize_pack_sym"] = {"us": sym_s * 1e6, "bytes": qb, "GB/s": qb / sym_s / 1e9,
+                                        "frac_hbm": qb / sym_s / 1e9 / peaks["hbm_gbs"], "launches": steps}
+        kernels["dequantize_bf16"] = {"us": dq_s * 1e6, "bytes": dqb, "GB/s": dqb / dq_s / 1e9,
+                                      "frac_hbm": dqb / dq_s / 1e9 / peaks["hbm_gbs"], "launches": steps,
+                                      "rotation": f"{cm} packed copies, {co} output copies",
+                                      "traffic": profiled_traffic("dequantize", args.workload)}
+        del outs
+
     # End to end through the public API with host buffers (pinned), copies inside.
     Wh = torch.from_numpy(W).pin_memory()
     Ah = torch.from_numpy(A.view(np.int16)).pin_memory()
@@ -484,6 +532,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="rows of W in the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip timing the symmetric quantizer and the explicit dequantize")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
