@@ -296,6 +296,23 @@ def test_matmul_k_zero_fills_zeros(env):
     assert torch.all(Y == 0)
 
 
+def test_binding_rejects_mismatched_tables(env):
+    """The C ABI takes bare pointers, so the binding checks the packed tables' shapes,
+    dtypes and contiguity before any launch; nothing reaches the GPU."""
+    torch, w4, _ = env
+    q = torch.zeros((4, 128), dtype=torch.uint8, device="cuda")
+    s = torch.ones((4, 2), dtype=torch.float16, device="cuda")
+    z = torch.zeros((4, 2), dtype=torch.uint8, device="cuda")
+    A = torch.zeros((2, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        w4.matmul(A, q, s[:, :1].contiguous(), z)
+    with pytest.raises(ValueError):
+        w4.dequantize(q, s, z[:3].contiguous())
+    with pytest.raises(ValueError):
+        w4.quantize_pack(torch.zeros((4, 256), dtype=torch.float16, device="cuda"), out=(q, s, z.t()))
+    assert w4.w4_check_device_error(0) == 0
+
+
 def test_empty_problems_are_noops(env):
     torch, w4, _ = env
     W = torch.empty((0, 256), dtype=torch.float16, device="cuda")

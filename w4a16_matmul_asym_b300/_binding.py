@@ -118,6 +118,20 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream)
 
 
+def _check_tables(qweight, scales, zeros, N: int, K: int, group: int, device) -> None:
+    """The packed tables must be contiguous CUDA tensors of the documented dtypes and
+    shapes on `device`: the C ABI takes bare pointers and cannot check their sizes, so a
+    wrong shape here would let a kernel read or write past a buffer."""
+    import torch
+    ng = K // group if group > 0 else 0
+    for name, t, dt, shape in (("qweight", qweight, torch.uint8, (N, K // 2)),
+                               ("scales", scales, torch.float16, (N, ng)),
+                               ("zeros", zeros, torch.uint8, (N, ng))):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != device:
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape} on {device}, "
+                             f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
 def quantize_pack(W, group: int = GROUP_SIZE, stream=None, out=None, symmetric: bool = False):
     """Quantize a CUDA tensor W[N,K] (float16 or float32).
 
@@ -143,6 +157,7 @@ def quantize_pack(W, group: int = GROUP_SIZE, stream=None, out=None, symmetric: 
         zeros = torch.empty((N, ng), dtype=torch.uint8, device=W.device)
     else:
         qweight, scales, zeros = out
+        _check_tables(qweight, scales, zeros, N, K, group, W.device)
     fn, name = (w4_quantize_pack_sym, "w4_quantize_pack_sym") if symmetric else (w4_quantize_pack, "w4_quantize_pack")
     rc = fn(W.data_ptr(), dt, N, K, group, qweight.data_ptr(), scales.data_ptr(), zeros.data_ptr(),
             _stream_handle(stream))
@@ -166,6 +181,7 @@ def dequantize(qweight, scales, zeros, dtype=None, group: int = GROUP_SIZE, stre
     if scales.dtype != torch.float16 or zeros.dtype != torch.uint8:
         raise TypeError("scales must be float16 and zeros uint8")
     N, K = qweight.shape[0], qweight.shape[1] * 2
+    _check_tables(qweight, scales, zeros, N, K, group, qweight.device)
     if out is None:
         out = torch.empty((N, K), dtype=dtype, device=qweight.device)
     elif out.dtype != dtype or tuple(out.shape) != (N, K) or not out.is_contiguous() or out.device != qweight.device:
@@ -189,6 +205,7 @@ def matmul(A, qweight, scales, zeros, group: int = GROUP_SIZE, stream=None, out=
         raise TypeError("qweight/zeros must be uint8 and scales float16")
     if tuple(qweight.shape) != (N, K // 2):
         raise ValueError(f"qweight shape {tuple(qweight.shape)} does not match K={K}")
+    _check_tables(qweight, scales, zeros, N, K, group, A.device)
     if out is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     else:
