@@ -2,22 +2,36 @@
 """Benchmark of the W4A16 hot path on one B300 (or N independent replicas).
 
 One step = w4_quantize_pack(W) followed by w4_matmul(A, qweight, scales, zeros) on
-the Llama-7B-shaped decode workload (W fp16 [11008, 4096] ~ N(0, 0.02) with 0.1% of
-entries x10, group 128; A bf16 [1, 4096] ~ N(0, 1)); other workloads via --workload.
+the 70B-scale MLP layer (W fp16 [28672, 8192] ~ N(0, 0.015^2) with 0.1% of entries
+x10, group 128; A bf16 [1, 8192] ~ N(0, 1)); another step workload via --workload.
 
 value      algorithmic GB/s of the whole step (quantize bytes W + qweight + scales +
            zeros, plus matmul bytes qweight + scales + zeros + A + Y) over the device
            time of K steps, inputs resident in HBM.  The K quantize launches and then the
            K matmul launches run as CUDA graphs (no host work between launches) between
-           CUDA events on the launching stream; L2 never serves a launch's weights: the
-           inputs rotate through copies spanning >= 3x the L2 size (launch i uses copy
-           i mod C), and step i's matmul reads the packed weights step i's quantize wrote.
-roofline   the kernel with the largest share of the step: its algorithmic bytes (or
-           flops for the tensor-core GEMM) per launch over its average launch duration
-           (its phase's event time / K), against the measured HBM (or bf16) peak.
-e2e        the same metric through the public API with host buffers: every step
+           CUDA events on the launching stream; step i's matmul reads the packed weights
+           step i's quantize wrote.
+kernels    every workload's kernels timed the same way (K launches each): the decode
+           GEMV on the Llama-7B shape, the M = 8 skinny GEMM, the prefill tcgen05 GEMM
+           and their quantize launches, plus the symmetric quantizer and the explicit
+           dequantize on the step workload; each with its fraction of the measured peak
+           and the bar it is held to.
+roofline   the step's dominant kernel (the larger share of the step's device time): its
+           algorithmic bytes per launch over its average launch duration, against the
+           measured HBM copy bandwidth.  roofline_tensor: the same for the prefill GEMM's
+           flops against the measured dense-bf16 peak.
+e2e        the same step metric through the public API with host buffers: every step
            copies W and A from pinned host memory, runs both calls, and reads Y back.
 cpu_baseline  the CPU oracle (plain C, one thread) on a bounded sample of the workload.
+
+Timing of one phase (K launches of one kernel): the launches are captured as CUDA
+graphs (one graph of exactly K launches, or repeats of one graph plus a remainder
+graph when K is large); every graph that is timed is replayed untimed first; then
+L2 is flushed by writing a buffer twice its size, a sleep kernel holds the stream
+while the host enqueues the events and the replays (so no host delay falls inside
+the event window), and CUDA events on the launching stream bracket the replays.
+L2 never serves a launch's inputs: they rotate through copies spanning >= 3x L2
+(launch i uses copy i mod C).
 
 --impl reference times that oracle alone (the reference arm).  Under torchrun each
 rank runs its own replica (weak scaling; no data-path collective); rank 0 prints the
@@ -27,8 +41,8 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import math
 import json
+import math
 import os
 import re
 import statistics
@@ -41,18 +55,32 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "W4A16 matmul HBM GB/s & TFLOP/s vs B300 roofline; quantize-pack GB/s"
-DEFAULT_WORKLOAD = "llama7b_gemv"
+DEFAULT_WORKLOAD = "mlp70b"
+OTHER_WORKLOADS = ["llama7b_gemv", "skinny_m8", "prefill_gemm"]
 ROTATE_L2 = 3              # rotating input copies span >= 3x the L2 size
 MAX_COPIES = 64            # cap for tiny inputs (the correctness-only configuration)
-LAUNCHES_PER_GRAPH = 50    # launches per captured CUDA graph (rounded to the copy cycle)
+MAX_GRAPH = 1000           # launches per captured CUDA graph at most
+SLEEP_CYCLES = 4_000_000   # ~2 ms sleep kernel ahead of each event window
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
+CSRC = "w4a16_matmul_asym_b300/csrc/"
 KERNEL_SOURCES = {  # every file a kernel is compiled from (its digest dates a profile)
-    "quantize_pack": ["w4a16_matmul_asym_b300/csrc/quantize_pack.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
-    "gemv": ["w4a16_matmul_asym_b300/csrc/gemv_dp4a.cuh", "w4a16_matmul_asym_b300/csrc/gemv.cuh",
-             "w4a16_matmul_asym_b300/csrc/common.cuh"],
-    "gemm_tcgen05": ["w4a16_matmul_asym_b300/csrc/gemm_tcgen05.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
-    "dequantize": ["w4a16_matmul_asym_b300/csrc/dequantize.cuh", "w4a16_matmul_asym_b300/csrc/common.cuh"],
+    "quantize_pack": [CSRC + "quantize_pack.cuh", CSRC + "common.cuh"],
+    "gemv": [CSRC + "gemv_dp4a.cuh", CSRC + "gemv.cuh", CSRC + "common.cuh"],
+    "gemv_mma": [CSRC + "gemv_mma.cuh", CSRC + "common.cuh"],
+    "gemm_tcgen05": [CSRC + "gemm_tcgen05.cuh", CSRC + "common.cuh"],
+    "dequantize": [CSRC + "dequantize.cuh", CSRC + "common.cuh"],
+}
+# The target fraction of each kernel's roofline per workload: (fraction, of which peak)
+BARS = {
+    ("quantize_pack", "mlp70b"): (0.60, "hbm"),
+    ("quantize_pack", "llama7b_gemv"): (0.60, "hbm"),
+    ("quantize_pack", "skinny_m8"): (0.60, "hbm"),
+    ("quantize_pack", "prefill_gemm"): (0.60, "hbm"),
+    ("matmul", "mlp70b"): (0.70, "hbm"),
+    ("matmul", "llama7b_gemv"): (0.70, "hbm"),
+    ("matmul", "skinny_m8"): (0.70, "hbm"),
+    ("matmul", "prefill_gemm"): (0.50, "bf16"),
 }
 
 
@@ -73,6 +101,12 @@ def matmul_flops(M: int, N: int, K: int) -> int:
     return 2 * M * N * K
 
 
+def dequantize_bytes(N: int, K: int) -> int:
+    """qweight + scales + zeros read, bf16 W_hat written."""
+    ng = K // 128
+    return N * K // 2 + 3 * N * ng + 2 * N * K
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -83,11 +117,20 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def matmul_kernel_name(M: int, K: int) -> str:
+    """Which kernel family w4_matmul runs for this shape (mirrors the dispatch)."""
+    if M > 8:
+        return "gemm_tcgen05"
+    return "gemv"
+
+
 def source_digest(kernel: str) -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        path = os.path.join(ROOT, rel)
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -104,6 +147,24 @@ def profiled_traffic(kernel: str, workload: str):
     if not m_src or not m_tr or m_src.group(1) != source_digest(kernel):
         return None
     return int(m_tr.group(1))
+
+
+def host_cpu():
+    """(cores this process may run on, CPU model name)."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return cores, model
 
 
 # ---- distributed control plane (CPU gloo; no data-path collective) ---------------------
@@ -141,6 +202,20 @@ def barrier(dist):
         dist.barrier()
 
 
+# ---- graph sizing ------------------------------------------------------------------------
+def graph_plan(count: int, period: int, max_graph: int = MAX_GRAPH):
+    """How `count` launches are split into captured graphs: (n, reps, rest) with
+    reps graphs of n launches and one of `rest` (n a multiple of `period`, so every
+    replay continues the copy rotation, unless count itself fits one graph)."""
+    if count <= 0:
+        return 0, 0, 0
+    if count <= max_graph:
+        return count, 1, 0
+    n = period * max(1, max_graph // period)
+    reps, rest = divmod(count, n)
+    return n, reps, rest
+
+
 # ---- clocks ---------------------------------------------------------------------------
 class ClockSampler:
     """Samples the SM clock and the clock-event (throttle) reasons while running:
@@ -153,7 +228,7 @@ class ClockSampler:
         0x100: "display_clock_setting",
     }
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, period_s: float = 0.02):
         self.period = period_s
         self.index = device_index
         self.samples, self.reasons = [], set()
@@ -161,6 +236,7 @@ class ClockSampler:
         self.error = None
         self.source = None
         self._stop = threading.Event()
+        self._first = threading.Event()
         self._thread = None
         self.nv = None
         try:
@@ -202,11 +278,15 @@ class ClockSampler:
                 self._sample_nvml() if self.nv is not None else self._sample_smi()
             except Exception as e:
                 self.error = f"{type(e).__name__}: {e}"
+            self._first.set()
             time.sleep(self.period)
 
     def start(self):
+        """Starts sampling and returns once the first sample is taken, so that the
+        sampler's start-up never overlaps an event window."""
         self._thread = threading.Thread(target=self._run, daemon=True)
         self._thread.start()
+        self._first.wait(timeout=10)
 
     def stop(self):
         if self._thread is not None:
@@ -246,6 +326,146 @@ def oracle_sample_rate(workload: str, budget_s: float, max_rows: int | None = No
 
 
 # ---- our arm --------------------------------------------------------------------------
+class PhaseTimer:
+    """Times `count` back-to-back launches of one kernel (see the module docstring)."""
+
+    def __init__(self, torch, dev, stream, l2_bytes: int):
+        self.torch = torch
+        self.dev = dev
+        self.stream = stream
+        self.cap = torch.cuda.Stream(dev)
+        self.flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        self.launches = 0          # our kernels launched inside event windows
+
+    def time(self, launch, count: int, warmup: int, period: int):
+        """Seconds per launch; launch(i, stream) enqueues launch i on `stream`."""
+        torch = self.torch
+        n, reps, rest = graph_plan(count, period)
+
+        def graph_of(k):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.cap):
+                for i in range(k):
+                    launch(i, self.cap)
+            return g
+
+        g_main = graph_of(n)
+        g_rest = graph_of(rest) if rest else None
+        done = 0
+        while True:                      # every timed graph replayed, >= warmup launches
+            g_main.replay()
+            done += n
+            if g_rest is not None:
+                g_rest.replay()
+                done += rest
+            if done >= warmup:
+                break
+        self.flush_buf.zero_()
+        torch.cuda.synchronize(self.dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(SLEEP_CYCLES)
+        a.record(self.stream)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rest is not None:
+            g_rest.replay()
+        b.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        self.launches += count
+        del g_main, g_rest
+        return a.elapsed_time(b) / 1e3 / count, {"graph_launches": n, "replays": reps, "remainder": rest}
+
+
+def copies_for(nbytes: int, l2: int) -> int:
+    return min(MAX_COPIES, max(2, -(-ROTATE_L2 * l2 // max(1, nbytes))))
+
+
+def hbm_entry(us_s: float, nbytes: int, peaks, bar=None, **extra):
+    gbs = nbytes / us_s / 1e9
+    d = {"us": us_s * 1e6, "bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+    if bar is not None:
+        d["bar"] = bar
+        d["meets_bar"] = d["frac_hbm"] >= bar
+    d.update(extra)
+    return d
+
+
+def run_workload(w4, torch, np, synth, timer, wl_name, steps, warmup, l2, peaks, step_workload,
+                 extras):
+    """Quantize and matmul launches of one workload (and, for the step workload, the
+    extra kernels).  Returns (kernels dict, phase seconds, info)."""
+    dev = timer.dev
+    wl = synth.WORKLOADS[wl_name]
+    N, K = wl.N, wl.K
+    W, A = synth.make_workload(wl_name)
+    M = A.shape[0]
+    qb, mb = quantize_bytes(N, K, W.dtype.itemsize), matmul_bytes(M, N, K)
+    qsz = N * K // 2 + 3 * N * (K // 128)
+    cw, cm = copies_for(W.nbytes, l2), copies_for(qsz, l2)
+    period = cw * cm // math.gcd(cw, cm)
+    Wds = [torch.from_numpy(W).to(dev) for _ in range(cw)]
+    Ad = torch.from_numpy(A.view(np.int16)).to(dev).view(torch.bfloat16)
+    qs = [torch.empty((N, K // 2), dtype=torch.uint8, device=dev) for _ in range(cm)]
+    ss = [torch.empty((N, K // 128), dtype=torch.float16, device=dev) for _ in range(cm)]
+    zs = [torch.empty((N, K // 128), dtype=torch.uint8, device=dev) for _ in range(cm)]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for i in range(cm):
+        w4.quantize_pack(Wds[i % cw], out=(qs[i], ss[i], zs[i]))
+    torch.cuda.synchronize(dev)
+
+    def q_launch(i, s_):
+        w4.quantize_pack(Wds[i % cw], out=(qs[i % cm], ss[i % cm], zs[i % cm]), stream=s_)
+
+    def m_launch(i, s_):
+        w4.matmul(Ad, qs[i % cm], ss[i % cm], zs[i % cm], out=Y, stream=s_)
+
+    q_s, q_graph = timer.time(q_launch, steps, warmup, period)
+    m_s, m_graph = timer.time(m_launch, steps, warmup, period)
+    mk = matmul_kernel_name(M, K)
+    rot = f"{cw} copies of W ({cw * W.nbytes / 1e6:.0f} MB), {cm} packed copies ({cm * qsz / 1e6:.0f} MB)"
+    ks = {"quantize_pack": hbm_entry(q_s, qb, peaks, BARS.get(("quantize_pack", wl_name), (None,))[0],
+                                     launches=steps, graphs=q_graph,
+                                     traffic=profiled_traffic("quantize_pack", wl_name))}
+    bar = BARS.get(("matmul", wl_name))
+    if mk == "gemm_tcgen05":
+        fl = matmul_flops(M, N, K)
+        tf = fl / m_s / 1e12
+        ent = {"kernel": mk, "us": m_s * 1e6, "flops": fl, "TFLOP/s": tf,
+               "frac_bf16_burst": tf / peaks["bf16_tflops"],
+               "frac_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
+               "GB/s": mb / m_s / 1e9, "launches": steps, "graphs": m_graph,
+               "traffic": profiled_traffic(mk, wl_name)}
+        if bar:
+            ent["bar"] = bar[0]
+            ent["meets_bar"] = ent["frac_bf16_burst"] >= bar[0]
+    else:
+        ent = hbm_entry(m_s, mb, peaks, bar[0] if bar else None, kernel=mk, launches=steps,
+                        graphs=m_graph, traffic=profiled_traffic(mk, wl_name))
+    ks["matmul"] = ent
+    info = {"N": N, "K": K, "M": M, "w_dtype": wl.w_dtype, "rotation": rot, "qb": qb, "mb": mb}
+
+    if extras and wl_name == step_workload:
+        out_bytes = N * K * 2
+        co = copies_for(out_bytes, l2)
+        outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(co)]
+        sym_s, _ = timer.time(lambda i, s_: w4.quantize_pack(
+            Wds[i % cw], out=(qs[i % cm], ss[i % cm], zs[i % cm]), stream=s_, symmetric=True),
+            steps, warmup, period)
+        dq_period = cm * co // math.gcd(cm, co)
+        dq_s, _ = timer.time(lambda i, s_: w4.dequantize(
+            qs[i % cm], ss[i % cm], zs[i % cm], dtype=torch.bfloat16, out=outs[i % co], stream=s_),
+            steps, warmup, dq_period)
+        ks["quantize_pack_sym"] = hbm_entry(sym_s, qb, peaks, launches=steps)
+        ks["dequantize_bf16"] = hbm_entry(dq_s, dequantize_bytes(N, K), peaks, launches=steps,
+                                          rotation=f"{cm} packed copies, {co} output copies",
+                                          traffic=profiled_traffic("dequantize", wl_name))
+        del outs
+    del Wds, qs, ss, zs, Y, Ad
+    torch.cuda.empty_cache()
+    return ks, (q_s, m_s), info
+
+
 def run_ours(args, ws, rank, local, dist):
     import numpy as np
     import torch
@@ -254,174 +474,67 @@ def run_ours(args, ws, rank, local, dist):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = synth.WORKLOADS[args.workload]
-    N, K = wl.N, wl.K
-    W, A = synth.make_workload(args.workload)
-    M = A.shape[0]
-    isz = W.dtype.itemsize
-    qb, mb = quantize_bytes(N, K, isz), matmul_bytes(M, N, K)
-    step_bytes = qb + mb
-    gemm = M > 8
-    mm_name = "gemm_tcgen05" if gemm else "gemv"
-
-    # L2 must not serve the timed launches: every launch reads a copy of its inputs that
-    # the launches before it have evicted.  W is replicated for the quantize launches and
-    # the packed weights for the matmul launches, each set >= 3x the L2 size, and launch
-    # i uses copy i mod C.  Step i's quantize writes the packed copy its matmul reads.
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20) or (126 << 20)
-    w_bytes = W.nbytes
-    qsz_bytes = N * K // 2 + 3 * N * (K // 128)
-    cw = min(MAX_COPIES, max(2, -(-ROTATE_L2 * l2 // w_bytes)))
-    cm = min(MAX_COPIES, max(2, -(-ROTATE_L2 * l2 // qsz_bytes)))
-    l2_defeated = cw * w_bytes >= ROTATE_L2 * l2 and cm * qsz_bytes >= ROTATE_L2 * l2
-    lcm = cw * cm // math.gcd(cw, cm)
-    R = lcm * max(1, -(-LAUNCHES_PER_GRAPH // lcm))          # launches per captured graph
-    steps = args.steps
-    n_rep, rem = divmod(steps, R)
-
-    Wh = torch.from_numpy(W)
-    Wds = [Wh.to(dev) for _ in range(cw)]
-    Ad = torch.from_numpy(A.view(np.int16)).to(dev).view(torch.bfloat16)
-    qs = [torch.empty((N, K // 2), dtype=torch.uint8, device=dev) for _ in range(cm)]
-    ss = [torch.empty((N, K // 128), dtype=torch.float16, device=dev) for _ in range(cm)]
-    zs = [torch.empty((N, K // 128), dtype=torch.uint8, device=dev) for _ in range(cm)]
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    Wd, q, s, z = Wds[0], qs[0], ss[0], zs[0]
     stream = torch.cuda.current_stream(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20) or (126 << 20)
+    peaks, peak_src = measured_peaks()
+    timer = PhaseTimer(torch, dev, stream, l2)
+    steps, warmup = args.steps, args.warmup
+    step_wl = args.workload
 
-    def step():
-        w4.quantize_pack(Wd, out=(q, s, z), stream=stream)
-        w4.matmul(Ad, q, s, z, out=Y, stream=stream)
-
-    # Both phases as CUDA graphs of R launches (no host work between launches).
-    for i in range(cm):
-        w4.quantize_pack(Wds[i % cw], out=(qs[i], ss[i], zs[i]), stream=stream)
-    w4.matmul(Ad, qs[0], ss[0], zs[0], out=Y, stream=stream)
-    torch.cuda.synchronize(dev)
-    cap = torch.cuda.Stream(dev)
-
-    def capture(n):
-        """(quantize graph, matmul graph) of n launches starting at copy 0."""
-        g_q, g_m = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_q, stream=cap):
-            for i in range(n):
-                w4.quantize_pack(Wds[i % cw], out=(qs[i % cm], ss[i % cm], zs[i % cm]), stream=cap)
-        with torch.cuda.graph(g_m, stream=cap):
-            for i in range(n):
-                w4.matmul(Ad, qs[i % cm], ss[i % cm], zs[i % cm], out=Y, stream=cap)
-        return g_q, g_m
-
-    # R is a multiple of both copy counts, so every replay continues the rotation.
-    g_q, g_m = capture(R)
-    g_qr, g_mr = capture(rem) if rem else (None, None)
-    for _ in range(max(1, -(-args.warmup // R))):   # >= warmup untimed steps
-        g_q.replay()
-        g_m.replay()
-    torch.cuda.synchronize(dev)
-
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     sampler = ClockSampler(torch.cuda.current_device())
     barrier(dist)
-    torch.cuda.synchronize(dev)
     sampler.start()
-    ev[0].record(stream)
-    for _ in range(n_rep):
-        g_q.replay()
-    if g_qr is not None:
-        g_qr.replay()
-    ev[1].record(stream)
-    for _ in range(n_rep):
-        g_m.replay()
-    if g_mr is not None:
-        g_mr.replay()
-    ev[2].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(dist)
+    kernels, step_info = {}, None
+    plan = [step_wl] + ([w for w in OTHER_WORKLOADS if w != step_wl] if not args.no_extra else [])
+    for name in plan:
+        ks, (q_s, m_s), info = run_workload(w4, torch, np, synth, timer, name, steps, warmup, l2,
+                                            peaks, step_wl, not args.no_extra)
+        kernels[name] = ks
+        if name == step_wl:
+            step_info, step_q, step_m = info, q_s, m_s
     clocks = sampler.stop()
-    launches = 2 * steps
-    q_total = ev[0].elapsed_time(ev[1]) / 1e3
-    m_total = ev[1].elapsed_time(ev[2]) / 1e3
-    local_s = q_total + m_total
+    barrier(dist)
+
+    N, K, M = step_info["N"], step_info["K"], step_info["M"]
+    step_bytes = step_info["qb"] + step_info["mb"]
+    local_s = (step_q + step_m) * steps
     tot_s, tot_bytes = aggregate(local_s, step_bytes * steps, dist)
     value = tot_bytes / tot_s / 1e9
 
-    peaks, peak_src = measured_peaks()
-    q_avg = q_total / steps
-    m_avg = m_total / steps
-    kernels = {
-        "quantize_pack": {"us": q_avg * 1e6, "bytes": qb, "GB/s": qb / q_avg / 1e9,
-                          "frac_hbm": qb / q_avg / 1e9 / peaks["hbm_gbs"]},
-        mm_name: {"us": m_avg * 1e6, "bytes": mb, "GB/s": mb / m_avg / 1e9,
-                  "frac_hbm": mb / m_avg / 1e9 / peaks["hbm_gbs"]},
-    }
-    if gemm:
-        fl = matmul_flops(M, N, K)
-        kernels[mm_name]["TFLOP/s"] = fl / m_avg / 1e12
-        kernels[mm_name]["frac_bf16_burst"] = fl / m_avg / 1e12 / peaks["bf16_tflops"]
-        kernels[mm_name]["frac_bf16_sustained"] = fl / m_avg / 1e12 / peaks["bf16_tflops_sustained"]
-    # Dominant kernel: the larger share of the step's device time.
-    if q_avg >= m_avg:
-        dom, ach, unit, peak, bound = "quantize_pack", qb / q_avg / 1e9, "GB/s", peaks["hbm_gbs"], "hbm"
-    elif gemm:
-        dom, unit, bound = mm_name, "TFLOP/s", "tensor"
-        ach, peak = matmul_flops(M, N, K) / m_avg / 1e12, peaks["bf16_tflops"]
+    sk = kernels[step_wl]
+    if step_q >= step_m:
+        dom, ent = "quantize_pack", sk["quantize_pack"]
     else:
-        dom, ach, unit, peak, bound = mm_name, mb / m_avg / 1e9, "GB/s", peaks["hbm_gbs"], "hbm"
-    roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
-                "frac": ach / peak, "peak_source": peak_src,
-                "traffic": profiled_traffic(dom, args.workload)}
-
-    # The two further kernels (not part of the step): the symmetric quantizer on the
-    # same W copies, and the explicit dequantize of the packed copies into rotating
-    # bf16 outputs; same method (CUDA graphs of back-to-back launches, events around
-    # `steps` launches per kernel, inputs and outputs rotated over >= 3x L2).
-    if not args.no_extra:
-        out_bytes = N * K * 2
-        co = min(MAX_COPIES, max(2, -(-ROTATE_L2 * l2 // out_bytes)))
-        outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(co)]
-
-        def time_phase(launch_i, period):
-            n = period * max(1, -(-LAUNCHES_PER_GRAPH // period))
-            reps, rest = divmod(steps, n)
-
-            def graph_of(count):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
-                    for i in range(count):
-                        launch_i(i, cap)
-                return g
-            g_full = graph_of(n)
-            g_rest = graph_of(rest) if rest else None
-            g_full.replay()
-            torch.cuda.synchronize(dev)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(reps):
-                g_full.replay()
-            if g_rest is not None:
-                g_rest.replay()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            return a.elapsed_time(b) / 1e3 / steps
-
-        sym_s = time_phase(lambda i, s_: w4.quantize_pack(Wds[i % cw], out=(qs[i % cm], ss[i % cm], zs[i % cm]),
-                                                          stream=s_, symmetric=True), R)
-        dq_period = cm * co // math.gcd(cm, co)
-        dq_s = time_phase(lambda i, s_: w4.dequantize(qs[i % cm], ss[i % cm], zs[i % cm], dtype=torch.bfloat16,
-                                                      out=outs[i % co], stream=s_), dq_period)
-        dqb = qsz_bytes + out_bytes
-        kernels["quantize_pack_sym"] = {"us": sym_s * 1e6, "bytes": qb, "GB/s": qb / sym_s / 1e9,
-                                        "frac_hbm": qb / sym_s / 1e9 / peaks["hbm_gbs"], "launches": steps}
-        kernels["dequantize_bf16"] = {"us": dq_s * 1e6, "bytes": dqb, "GB/s": dqb / dq_s / 1e9,
-                                      "frac_hbm": dqb / dq_s / 1e9 / peaks["hbm_gbs"], "launches": steps,
-                                      "rotation": f"{cm} packed copies, {co} output copies",
-                                      "traffic": profiled_traffic("dequantize", args.workload)}
-        del outs
+        dom, ent = sk["matmul"].get("kernel", "matmul"), sk["matmul"]
+    if "TFLOP/s" in ent:
+        roofline = {"bound": "tensor", "kernel": dom, "workload": step_wl, "achieved": ent["TFLOP/s"],
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ent["frac_bf16_burst"],
+                    "peak_source": peak_src, "traffic": ent.get("traffic")}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom, "workload": step_wl, "achieved": ent["GB/s"],
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ent["frac_hbm"],
+                    "peak_source": peak_src, "traffic": ent.get("traffic")}
+    roofline_tensor = None
+    if "prefill_gemm" in kernels:
+        g = kernels["prefill_gemm"]["matmul"]
+        roofline_tensor = {"bound": "tensor", "kernel": g.get("kernel"), "workload": "prefill_gemm",
+                           "achieved": g.get("TFLOP/s"), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": g.get("frac_bf16_burst"), "peak_source": peak_src,
+                           "peak_sustained": peaks["bf16_tflops_sustained"],
+                           "frac_sustained": g.get("frac_bf16_sustained"), "traffic": g.get("traffic")}
 
     # End to end through the public API with host buffers (pinned), copies inside.
+    wl = synth.WORKLOADS[step_wl]
+    W, A = synth.make_workload(step_wl)
     Wh = torch.from_numpy(W).pin_memory()
     Ah = torch.from_numpy(A.view(np.int16)).pin_memory()
     Yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    Wd = torch.empty_like(Wh, device=dev)
+    Ad = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+    z = torch.empty((N, K // 128), dtype=torch.uint8, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     e2e_steps = max(3, min(args.steps, 50))
     h2d = Wh.numel() * Wh.element_size() + Ah.numel() * Ah.element_size()
     d2h = Yh.numel() * Yh.element_size()
@@ -429,7 +542,8 @@ def run_ours(args, ws, rank, local, dist):
     def e2e_step():
         Wd.copy_(Wh, non_blocking=True)
         Ad.view(torch.int16).copy_(Ah, non_blocking=True)
-        step()
+        w4.quantize_pack(Wd, out=(q, s, z), stream=stream)
+        w4.matmul(Ad, q, s, z, out=Y, stream=stream)
         Yh.copy_(Y, non_blocking=True)
 
     for _ in range(2):
@@ -448,35 +562,36 @@ def run_ours(args, ws, rank, local, dist):
 
     result = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": tot_s / steps * 1e3,
+        "steps": steps, "warmup": warmup, "ms_per_step": tot_s / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "w4a16: int4 weights with fp16 scales, bf16 activations, fp32 accumulation "
+                 "(quantize in fp32)",
+        "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: {wl.desc}; group 128",
+            "workload": f"{step_wl}: {wl.desc}; group 128",
             "N": N, "K": K, "M": M, "group": 128, "w_dtype": wl.w_dtype,
             "step": "w4_quantize_pack + w4_matmul",
-            "l2": (f"not serving the timed launches: inputs larger than L2, rotated: {cw} copies of W "
-                   f"({cw * w_bytes / 1e6:.0f} MB) for the quantize launches, {cm} copies of the packed "
-                   f"weights ({cm * qsz_bytes / 1e6:.0f} MB) for the matmul launches, each set >= "
-                   f"{ROTATE_L2}x the {l2 / 2**20:.0f} MiB L2; launch i uses copy i mod C"
-                   if l2_defeated else
-                   f"tiny workload: {cw} / {cm} rotating copies do not span {ROTATE_L2}x L2 (correctness config)"),
-            "timing": (f"CUDA events around {steps} quantize launches, then around {steps} matmul launches "
-                       f"(CUDA graphs of {R} launches each; step i's matmul reads what step i's quantize "
-                       f"wrote); per-kernel time = phase time / steps"),
+            "l2": (f"inputs larger than L2 and rotated, each set >= {ROTATE_L2}x the "
+                   f"{l2 / 2**20:.0f} MiB L2 (step: {step_info['rotation']}); L2 flushed before "
+                   f"every event window"),
+            "timing": (f"per kernel: CUDA events around {steps} back-to-back launches replayed from "
+                       f"CUDA graphs (graphs of <= {MAX_GRAPH} launches, each replayed untimed before "
+                       f"the window); step = the quantize phase then the matmul phase, step i's matmul "
+                       f"reading what step i's quantize wrote"),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
         "roofline": roofline,
+        "roofline_tensor": roofline_tensor,
         "kernels": kernels,
         "e2e": e2e,
-        "gpu_launches": launches,
+        "gpu_launches": timer.launches,
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, desc, _, _ = oracle_sample_rate(args.workload, budget_s=args.cpu_budget,
-                                              max_rows=args.cpu_rows)
+        rate, desc, _, _ = oracle_sample_rate(step_wl, budget_s=args.cpu_budget, max_rows=args.cpu_rows)
+        cores, model = host_cpu()
         result["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                  "sample": desc}
+                                  "sample": desc, "host_cores": cores, "cpu_model": model}
     return result
 
 
@@ -504,6 +619,7 @@ def run_reference(args, ws, rank):
         step()
     secs = time.perf_counter() - t0
     value = nbytes * args.steps / secs / 1e9
+    cores, model = host_cpu()
     desc = (f"oracle quantize+matmul on the first {rows} of {wl.N} rows of the {args.workload} "
             f"workload per step (K={wl.K}, M={A.shape[0]}), 1 thread")
     return {
@@ -514,7 +630,7 @@ def run_reference(args, ws, rank):
         "config": {"workload": f"{args.workload}: {wl.desc}; group 128", "N": wl.N, "K": wl.K,
                    "M": wl.M, "group": 128, "sample_rows": rows},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "host_cores": cores, "cpu_model": model},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -523,20 +639,22 @@ def main(argv=None):
     import synth
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(synth.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU time for the oracle baseline")
-    ap.add_argument("--cpu-rows", type=int, default=2048,
+    ap.add_argument("--cpu-rows", type=int, default=1024,
                     help="rows of W in the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip timing the symmetric quantizer and the explicit dequantize")
+                    help="time the step workload only (no other workloads or extra kernels)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     ws, rank, local = dist_info()
     if args.impl == "reference":
         if rank == 0:

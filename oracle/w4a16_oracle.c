@@ -35,7 +35,7 @@
  *     Weights", "Key design decisions") names symmetric per-group scales as the
  *     standard choice for transformer weights.
  *
- * Readings taken where the pages are silent or disagree (listed in the design doc):
+ * Readings taken where the pages are silent or disagree:
  *   - q and zp are computed with the fp32 scale; only dequantization uses the
  *     stored fp16 scale.
  *   - q = clip(rint(w / s) + zp, 0, 15), i.e. rounding happens before adding zp

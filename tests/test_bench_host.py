@@ -70,3 +70,27 @@ def test_reference_arm_runs_on_cpu(capsys):
     d = json.loads(line)
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("count,period", [(1, 85), (20, 85), (20, 17), (999, 5), (1000, 85),
+                                          (1001, 85), (10000, 85), (10000, 7), (5000, 2000)])
+def test_graph_plan_covers_exactly_count_launches(count, period):
+    n, reps, rest = bench.graph_plan(count, period)
+    assert n * reps + rest == count
+    assert 0 < n <= max(bench.MAX_GRAPH, period)
+    if count > bench.MAX_GRAPH:
+        assert n % period == 0          # every full replay continues the copy rotation
+    else:
+        assert (n, reps, rest) == (count, 1, 0)
+
+
+def test_host_cpu_reports_cores_and_model():
+    cores, model = bench.host_cpu()
+    assert cores >= 1 and isinstance(model, str) and model
+
+
+def test_kernel_names_have_sources():
+    for M, K in ((1, 4096), (8, 4096), (2048, 4096), (1, 8192)):
+        name = bench.matmul_kernel_name(M, K)
+        assert name in bench.KERNEL_SOURCES
+        assert len(bench.source_digest(name)) == 16

@@ -100,6 +100,13 @@ def test_quantize_sym_fp32_wide_range(env):
     assert_sym_equal(env, W)
 
 
+def test_quantize_sym_fp32_tiny_scales(env):
+    """Symmetric groups with absmax below ~2e-38 (scale without a finite reciprocal),
+    including exact zeros, quantize bit-exactly."""
+    from test_gpu_parity import tiny_scale_rows
+    assert_sym_equal(env, tiny_scale_rows(np.random.default_rng(18)))
+
+
 # ---- dequantize ---------------------------------------------------------------------
 def run_dequant(env, q, s, z, dtype):
     torch, w4, _ = env

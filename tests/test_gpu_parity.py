@@ -143,6 +143,27 @@ def test_quantize_random_fp32_many_ties(env):
     assert_quant_equal(env, W)
 
 
+def tiny_scale_rows(rng):
+    """fp32 groups whose scale lies below 2^-128 (no finite reciprocal): subnormal and
+    tiny normal values, exact zeros among them; every range stays >= 1000 * 2^-149 so
+    the scale itself is nonzero."""
+    t = np.float32(2.0 ** -149)
+    rows = [
+        (rng.uniform(-1e-38, 1e-38, 128)).astype(np.float32),                  # subnormal s
+        (rng.uniform(0, 3e-39, 128)).astype(np.float32),                       # all positive
+        (rng.integers(-1000, 1001, 128).astype(np.float32) * t),               # s = 133 * 2^-149
+        np.where(rng.random(128) < 0.5, 0.0, rng.uniform(-4e-38, 4e-38, 128)).astype(np.float32),
+        (rng.uniform(-1e-37, 1e-37, 128)).astype(np.float32),                  # tiny normals
+        (rng.integers(-7, 8, 128).astype(np.float32) * np.float32(2.0 ** -130)),  # ties on a grid
+    ]
+    return np.stack(rows)
+
+
+def test_quantize_fp32_tiny_scales(env):
+    """Groups whose fp32 scale has no finite reciprocal still quantize bit-exactly."""
+    assert_quant_equal(env, tiny_scale_rows(np.random.default_rng(17)))
+
+
 # ---- matmul: GEMV / skinny path (M <= 8) ----------------------------------------------
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_matmul_small_m(env, M):
@@ -390,6 +411,18 @@ def test_matmul_gemm_output_guard(env, M, N, K, offset):
     Yref, S = orc.matmul(A, q, s, z)
     ok, worst, idx = orc.check_y(flat[pad:pad + M * N].reshape(M, N), Yref, S)
     assert ok, f"worst ratio {worst:.3g} at {idx}"
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 38400, 128), (300, 20000, 256)])
+def test_matmul_gemm_many_tiles_full(env, M, N, K):
+    """More than twice as many tiles as SMs at small K, every output compared: the
+    persistent tile loop (accumulator hand-off and barrier phases across many tiles
+    per CTA) checked element by element, not on a sample."""
+    import synth
+    _, _, orc = env
+    W, A = synth.make_random(N, K, M, seed=M + N + K)
+    q, s, z = orc.quantize_pack(W)
+    assert_matmul_ok(env, A, q, s, z)
 
 
 def test_matmul_prefill_workload_sampled(env):

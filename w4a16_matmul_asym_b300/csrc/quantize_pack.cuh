@@ -104,6 +104,7 @@ struct GroupParams {
     float r15;      // fl(1/15)
     float c15;      // fl(zp * fl(1/15))
     float zp;       // zero point (0..15) as float
+    bool exact;     // fl(1/s) overflowed (s < ~2^-128): every level by IEEE division
 };
 
 template <bool kSym>
@@ -121,6 +122,11 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
         p.zp = fminf(fmaxf(zq, 0.0f), 15.0f);
     }
     const float rcp = __frcp_rn(p.s);
+    // A scale below about 2^-128 (an fp32 group range under ~4.4e-38, or an absmax
+    // under ~2e-38 in the symmetric variant) has no finite reciprocal: t = w * rcp
+    // would be +-inf or NaN and the tie test below would not see it.  Such groups
+    // take the exact per-element division.
+    p.exact = (__float_as_uint(rcp) & 0x7f800000u) == 0x7f800000u;
     const float mz = __fadd_rn(kRoundMagic, p.zp);
     p.rcp2 = f2pack(rcp, rcp);
     p.mz2 = f2pack(mz, mz);
@@ -150,7 +156,7 @@ __device__ __forceinline__ uint32_t quantize8(const float (&w)[8], const GroupPa
     const uint64_t M22 = f2pack(4194304.0f, 4194304.0f);  // 2^22: L - 2^22 = 2^23 + q
     const uint64_t c15x2 = f2pack(15.0f, 15.0f);
     uint64_t t[4];
-    bool tie = false;
+    bool tie = p.exact;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         t[j] = f2mul(f2pack(w[j], w[j + 4]), p.rcp2);
