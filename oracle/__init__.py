@@ -1,8 +1,10 @@
 """CPU oracle (test infrastructure only): see oracle.py and w4a16_oracle.c."""
-from .oracle import (GROUP, REL_TOL, bf16_bits_to_f64, bf16_to_f64, build, check_y,
+from .oracle import (CALIB_METHODS, GROUP, REL_TOL, bf16_bits_to_f64, bf16_to_f64, build, check_y,
                      dequantize, dequantize16, f16_to_f32, f32_to_bf16_bits, f32_to_f16_bits,
-                     matmul, matmul_entries, quantize_pack, ulp_bf16, unpack, y_tolerance)
+                     matmul, matmul_entries, mse_step, percentile_abs, quantize_pack,
+                     quantize_pack_calibrated, ulp_bf16, unpack, y_tolerance)
 
-__all__ = ["GROUP", "REL_TOL", "bf16_bits_to_f64", "bf16_to_f64", "build", "check_y",
+__all__ = ["CALIB_METHODS", "GROUP", "REL_TOL", "bf16_bits_to_f64", "bf16_to_f64", "build", "check_y",
            "dequantize", "dequantize16", "f16_to_f32", "f32_to_bf16_bits", "f32_to_f16_bits",
-           "matmul", "matmul_entries", "quantize_pack", "ulp_bf16", "unpack", "y_tolerance"]
+           "matmul", "matmul_entries", "mse_step", "percentile_abs", "quantize_pack",
+           "quantize_pack_calibrated", "ulp_bf16", "unpack", "y_tolerance"]

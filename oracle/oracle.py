@@ -63,6 +63,13 @@ def _load():
     lib.oracle_quantize_pack.restype = ctypes.c_int
     lib.oracle_quantize_pack_sym.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
     lib.oracle_quantize_pack_sym.restype = ctypes.c_int
+    lib.oracle_quantize_pack_calib.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_double,
+                                               vp, vp, vp, vp]
+    lib.oracle_quantize_pack_calib.restype = ctypes.c_int
+    lib.oracle_percentile_abs.argtypes = [vp, ctypes.c_int, ctypes.c_float]
+    lib.oracle_percentile_abs.restype = ctypes.c_float
+    lib.oracle_mse_step.argtypes = [vp, ctypes.c_int, ctypes.c_int]
+    lib.oracle_mse_step.restype = ctypes.c_float
     lib.oracle_dequantize_16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, vp]
     lib.oracle_dequantize_16.restype = ctypes.c_int
     lib.oracle_f32_to_bf16_bits.argtypes = [ctypes.c_float]
@@ -127,6 +134,50 @@ def quantize_pack(W: np.ndarray, with_fp32_scales: bool = False, symmetric: bool
         raise RuntimeError(f"oracle_quantize_pack failed ({rc})")
     out = (q, s.view(np.float16), z)
     return out + (s32,) if with_fp32_scales else out
+
+
+CALIB_METHODS = {"percentile": 2, "mse": 3}
+
+
+def quantize_pack_calibrated(W: np.ndarray, method: str, param: float, with_fp32_scales: bool = False):
+    """Clip-range calibrated symmetric quantization of W[N,K] (float16 or float32):
+    method "percentile" (param = p, the percentile of |w| taken as the clip range) or
+    "mse" (param = number of linspace candidate steps).  Same outputs as
+    quantize_pack: levels clamp(rint(w / s), -7, 7) + 8, zero points 8, fp16 scales."""
+    if W.ndim != 2:
+        raise ValueError("W must be 2-D [N,K]")
+    N, K = W.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    if W.dtype == np.float16:
+        src, dt = _as_u16_bits(W), 0
+    elif W.dtype == np.float32:
+        src, dt = np.ascontiguousarray(W), 1
+    else:
+        raise TypeError("W must be float16 or float32")
+    ng = K // GROUP
+    q = np.empty((N, K // 2), np.uint8)
+    s = np.empty((N, ng), np.uint16)
+    z = np.empty((N, ng), np.uint8)
+    s32 = np.empty((N, ng), np.float32)
+    rc = _load().oracle_quantize_pack_calib(_ptr(src), dt, N, K, CALIB_METHODS[method], float(param),
+                                            _ptr(q), _ptr(s), _ptr(z), _ptr(s32))
+    if rc:
+        raise RuntimeError(f"oracle_quantize_pack_calib failed ({rc})")
+    out = (q, s.view(np.float16), z)
+    return out + (s32,) if with_fp32_scales else out
+
+
+def percentile_abs(group: np.ndarray, p: float) -> np.float32:
+    """The percentile calibrator's clip range for one group (fp32 values)."""
+    g = np.ascontiguousarray(group, dtype=np.float32)
+    return np.float32(_load().oracle_percentile_abs(_ptr(g), len(g), float(p)))
+
+
+def mse_step(group: np.ndarray, n: int) -> np.float32:
+    """The MSE calibrator's chosen step for one group (fp32 values)."""
+    g = np.ascontiguousarray(group, dtype=np.float32)
+    return np.float32(_load().oracle_mse_step(_ptr(g), len(g), int(n)))
 
 
 def unpack(qweight: np.ndarray, K: int) -> np.ndarray:

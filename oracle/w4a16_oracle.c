@@ -48,6 +48,23 @@
  *     (scale = absmax, quantizing |w|) loses the sign and is not followed.
  *   - Dequantized output as a 16-bit tensor: the exact product (q - zp) * s16
  *     rounded once to nearest-even bfloat16 or binary16.
+ *   - Clip-range calibration ("Building a From-Scratch Group-Wise INT4 Quantization
+ *     Layer for LLaMA Weights", Step 4, ScaleCalibrator), per group of 128 along K:
+ *       percentile: the clip range r is the p-th percentile of |w| with linear
+ *         interpolation between order statistics, in fp32: h = fl(fl(p / 100) * 127),
+ *         lo = floor(h), f = h - lo, r = a_lo + f * (a_lo+1 - a_lo) (two roundings);
+ *         the step is s = r / 7 (1 when r == 0), as the absmax calibrator's range
+ *         gives absmax / 7 (the page's listing divides by the range itself, which
+ *         leaves only the levels -1, 0, 1 and is not followed).
+ *       mse: the step itself is searched: candidates c_i = linspace(min|w|, max|w|, n)
+ *         in fp32 (c_i = fl(min + fl(i * step)), step = fl((max - min) / (n - 1)),
+ *         c_(n-1) = max exactly; n = 1 gives min); candidates below fl32(1e-10) are
+ *         skipped; each is scored by mean((clamp(rint(w / c), -7, 7) * c - w)^2)
+ *         summed in fp32 in index order, every product, difference and sum rounded
+ *         once; the first candidate with the smallest score wins (strict <), and 1e-8
+ *         when none is scored.
+ *     Both store level clamp(rint(w / s), -7, 7) + 8 with zero point 8 (the page's
+ *     [-7, 7] range) and the fp16-rounded step as the scale.
  */
 #include <math.h>
 #include <stdint.h>
@@ -189,6 +206,101 @@ static void quantize_group_sym(const float *w, int G, uint8_t *q, float *scale, 
     *zero = 8;
 }
 
+/* ---- clip-range calibration ---------------------------------------------------- */
+/* The page's symmetric level rule with the [-7, 7] range: level = q + 8. */
+static void levels_sym7(const float *w, int G, float s, uint8_t *q)
+{
+    for (int i = 0; i < G; ++i) {
+        float t = rintf(w[i] / s);
+        float c = fminf(fmaxf(t, -7.0f), 7.0f);
+        q[i] = (uint8_t)((int)c + 8);
+    }
+}
+
+/* p-th percentile (0 < p <= 100) of |w| over the group, linear interpolation between
+ * the order statistics (ascending a_0 <= ... <= a_(G-1)), in fp32. */
+float oracle_percentile_abs(const float *w, int G, float p)
+{
+    float a[ORACLE_GROUP];
+    for (int i = 0; i < G; ++i) a[i] = fabsf(w[i]);
+    for (int i = 1; i < G; ++i) {           /* insertion sort, ascending */
+        float v = a[i];
+        int j = i - 1;
+        while (j >= 0 && a[j] > v) {
+            a[j + 1] = a[j];
+            --j;
+        }
+        a[j + 1] = v;
+    }
+    float qf = p / 100.0f;
+    float h = qf * (float)(G - 1);
+    float fl = floorf(h);
+    int lo = (int)fl;
+    if (lo < 0) lo = 0;
+    if (lo > G - 1) lo = G - 1;
+    int hi = lo + 1 < G ? lo + 1 : G - 1;
+    float f = h - fl;                       /* exact */
+    float d = a[hi] - a[lo];
+    float fd = f * d;
+    return a[lo] + fd;
+}
+
+/* The step chosen by the MSE search over n candidates (see the header). */
+float oracle_mse_step(const float *w, int G, int n)
+{
+    float lo = fabsf(w[0]), hi = lo;
+    for (int i = 1; i < G; ++i) {
+        float a = fabsf(w[i]);
+        if (a < lo) lo = a;
+        if (a > hi) hi = a;
+    }
+    const float thr = 1e-10f;
+    float best_s = 1e-8f, best = INFINITY;
+    float step = (n > 1) ? (hi - lo) / (float)(n - 1) : 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float c;
+        if (n == 1) c = lo;
+        else if (i == n - 1) c = hi;
+        else {
+            float is = (float)i * step;
+            c = lo + is;
+        }
+        if (c < thr) continue;
+        float e = 0.0f;
+        for (int k = 0; k < G; ++k) {
+            float t = rintf(w[k] / c);
+            t = fminf(fmaxf(t, -7.0f), 7.0f);
+            float r = t * c;
+            float d = r - w[k];
+            float d2 = d * d;
+            e = e + d2;
+        }
+        float mse = e / (float)G;
+        if (mse < best) {
+            best = mse;
+            best_s = c;
+        }
+    }
+    return best_s;
+}
+
+/* Calibrated symmetric quantization of one group: method 2 = percentile (param = p),
+ * method 3 = MSE search (param = number of candidates). */
+static void quantize_group_calib(const float *w, int G, int method, double param, uint8_t *q,
+                                 float *scale, int *zero)
+{
+    float s;
+    if (method == 2) {
+        float r = oracle_percentile_abs(w, G, (float)param);
+        s = (r == 0.0f) ? 1.0f : r / 7.0f;
+    } else {
+        s = oracle_mse_step(w, G, (int)param);
+    }
+    levels_sym7(w, G, s, q);
+    *scale = s;
+    *zero = 8;
+}
+
 /* Quantize and pack W[N,K] (row-major, K contiguous).
  *   w_dtype: 0 = fp16 bits (uint16), 1 = fp32
  *   qweight: uint8 [N, K/2], element 2j in the low nibble, 2j+1 in the high nibble
@@ -196,7 +308,7 @@ static void quantize_group_sym(const float *w, int G, uint8_t *q, float *scale, 
  *   zeros  : uint8 [N, K/128]
  *   scales32 (optional, may be NULL): the fp32 scales, for tests of the bound.
  * Returns 0, or -1 on invalid arguments. */
-static int quantize_pack_mode(const void *W, int w_dtype, int64_t N, int64_t K, int symmetric,
+static int quantize_pack_mode(const void *W, int w_dtype, int64_t N, int64_t K, int mode, double param,
                               uint8_t *qweight, uint16_t *scales, uint8_t *zeros, float *scales32)
 {
     if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
@@ -215,8 +327,10 @@ static int quantize_pack_mode(const void *W, int w_dtype, int64_t N, int64_t K, 
             }
             float s;
             int zp;
-            if (symmetric)
+            if (mode == 1)
                 quantize_group_sym(wbuf, ORACLE_GROUP, qbuf, &s, &zp);
+            else if (mode >= 2)
+                quantize_group_calib(wbuf, ORACLE_GROUP, mode, param, qbuf, &s, &zp);
             else
                 quantize_group(wbuf, ORACLE_GROUP, qbuf, &s, &zp);
             scales[n * ng + g] = oracle_f32_to_f16_bits(s);
@@ -235,7 +349,7 @@ int oracle_quantize_pack(const void *W, int w_dtype, int64_t N, int64_t K,
                          uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
                          float *scales32)
 {
-    return quantize_pack_mode(W, w_dtype, N, K, 0, qweight, scales, zeros, scales32);
+    return quantize_pack_mode(W, w_dtype, N, K, 0, 0.0, qweight, scales, zeros, scales32);
 }
 
 /* The symmetric variant: same layouts, zero points all 8. */
@@ -243,7 +357,19 @@ int oracle_quantize_pack_sym(const void *W, int w_dtype, int64_t N, int64_t K,
                              uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
                              float *scales32)
 {
-    return quantize_pack_mode(W, w_dtype, N, K, 1, qweight, scales, zeros, scales32);
+    return quantize_pack_mode(W, w_dtype, N, K, 1, 0.0, qweight, scales, zeros, scales32);
+}
+
+/* Clip-range calibrated symmetric variant: method 2 = percentile with p = param
+ * (0 < p <= 100), method 3 = MSE search over (int)param >= 1 candidates. */
+int oracle_quantize_pack_calib(const void *W, int w_dtype, int64_t N, int64_t K, int method,
+                               double param, uint8_t *qweight, uint16_t *scales, uint8_t *zeros,
+                               float *scales32)
+{
+    if (method == 2 && !(param > 0.0 && param <= 100.0)) return -1;
+    if (method == 3 && !(param >= 1.0)) return -1;
+    if (method != 2 && method != 3) return -1;
+    return quantize_pack_mode(W, w_dtype, N, K, method, param, qweight, scales, zeros, scales32);
 }
 
 /* Unpack qweight[N,K/2] into q[N,K] (one value 0..15 per byte). */

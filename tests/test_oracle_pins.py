@@ -384,3 +384,136 @@ def test_dequantize16_is_the_exact_product_rounded_once(oracle_mod, out):
     else:
         ref = torch.from_numpy(exact).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, ref)
+
+
+# ---- clip-range calibration ("Building a From-Scratch Group-Wise INT4 Quantization Layer
+# for LLaMA Weights", Step 4) ------------------------------------------------------------
+def calib_group(name):
+    k = np.arange(128)
+    if name == "ramp":
+        return ((k + 1) / 128.0 * np.where(k % 2 == 0, 1.0, -1.0)).astype(np.float32)
+    if name == "grid":
+        base = np.concatenate([np.arange(1, 8), -np.arange(1, 8)]) / 64.0
+        return np.resize(base, 128).astype(np.float32)
+    if name == "constant":
+        return (np.float32(0.3) * np.where(k % 3 == 0, -1.0, 1.0)).astype(np.float32)
+    if name == "zeros":
+        return np.zeros(128, np.float32)
+    if name == "tie":
+        w = np.zeros(128, np.float32)
+        w[[0, 5]], w[1] = 1.0, -1.0
+        return w
+    raise KeyError(name)
+
+
+CALIB_CASES = parse_cases(os.path.join(GOLDEN_DIR, "calib_groups.txt"))
+
+
+@pytest.mark.parametrize("case", CALIB_CASES, ids=[c["name"] for c in CALIB_CASES])
+def test_calibration_hand_worked_groups(oracle_mod, case):
+    w = calib_group(case["values"])
+    param = float(case["param"])
+    if case["method"] == "percentile":
+        r = oracle_mod.percentile_abs(w, param)
+        assert r == np.float32(float(case["r"]))
+        s_exp = np.float32(1.0) if r == 0 else np.float32(r) / np.float32(7.0)
+    else:
+        s_exp = np.float32(float(case["s"]))
+        assert oracle_mod.mse_step(w, int(param)) == s_exp
+    q, s16, z, s32 = oracle_mod.quantize_pack_calibrated(w[None, :], case["method"], param,
+                                                         with_fp32_scales=True)
+    assert s32[0, 0] == s_exp and z[0, 0] == 8
+    assert s16[0, 0] == s_exp.astype(np.float16)
+    lv = oracle_mod.unpack(q, 128)[0].astype(np.int64)
+    if case["name"] == "grid_mse":
+        assert np.array_equal(lv - 8, np.rint(w * 64).astype(np.int64))
+    if case["name"] == "constant_mse":
+        assert np.array_equal(lv - 8, np.sign(w).astype(np.int64))
+    if case["name"] == "zeros_mse":
+        assert np.all(lv == 8)
+    if case["name"] == "tie_mse":
+        from fractions import Fraction
+        step = Fraction(float(np.float32(1.0) / np.float32(999.0)))
+        half_ulp = Fraction(1, 2 ** 26)          # fl(1/3) lies in [2^-2, 2^-1): ulp 2^-25
+        assert abs(333 * step - Fraction(float(s_exp))) < half_ulp
+        assert lv[0] == 11 and lv[1] == 5 and lv[5] == 11 and np.all(lv[2:5] == 8)
+
+
+def test_percentile_100_is_the_absmax_quantizer(oracle_mod):
+    """p = 100 takes the largest |w| as the range, s = absmax / 7: the pinned symmetric
+    quantizer (whose [-8, 7] clip never binds when s = absmax / 7)."""
+    rng = np.random.default_rng(51)
+    W = (rng.standard_normal((64, 512)) * 0.02).astype(np.float16)
+    W[3, :128] = 0
+    a = oracle_mod.quantize_pack_calibrated(W, "percentile", 100.0)
+    b = oracle_mod.quantize_pack(W, symmetric=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
+
+
+@pytest.mark.parametrize("p", [0.5, 10.0, 50.0, 90.0, 99.0, 99.9, 100.0])
+def test_percentile_matches_numpy_quantile(oracle_mod, p):
+    """Against numpy's linear-interpolation quantile in fp64 (a library routine): the
+    fp32 evaluation differs only by roundings, far below one order-statistic gap, so
+    a wrong rank, sort order or interpolation weight fails."""
+    rng = np.random.default_rng(int(p * 10) + 1)
+    for _ in range(50):
+        w = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 2)).astype(np.float32)
+        r = float(oracle_mod.percentile_abs(w, p))
+        ref = float(np.quantile(np.abs(w).astype(np.float64), p / 100.0, method="linear"))
+        assert abs(r - ref) <= 1e-6 * np.abs(w).max(), (p, r, ref)
+
+
+def _mse64(w, c):
+    """The search's score of step c, in fp64 with exact quotients (independent of the
+    fp32 evaluation order)."""
+    w = w.astype(np.float64)
+    lv = np.clip(np.rint(w / c), -7, 7)
+    return np.mean((lv * c - w) ** 2)
+
+
+def test_mse_choice_is_optimal_in_fp64(oracle_mod):
+    """The chosen step lies on the candidate grid linspace(min|w|, max|w|, n) and, with
+    its score recomputed in fp64, is within rounding of the best candidate's."""
+    rng = np.random.default_rng(61)
+    n = 1000
+    for trial in range(40):
+        w = (rng.standard_normal(128) * 0.02).astype(np.float32)
+        if trial % 4 == 0:
+            w[rng.integers(0, 128, 2)] *= 10            # outliers
+        s = float(oracle_mod.mse_step(w, n))
+        lo, hi = float(np.abs(w).min()), float(np.abs(w).max())
+        grid = lo + np.arange(n) * (hi - lo) / (n - 1)
+        i = int(np.argmin(np.abs(grid - s)))
+        assert abs(grid[i] - s) <= 4e-7 * hi
+        scores = np.array([_mse64(w, c) for c in grid])
+        best = scores.min()
+        assert _mse64(w, s) <= best * (1 + 1e-4) + 1e-30
+        # the first minimum: no candidate before the chosen one scores clearly better
+        assert np.all(scores[:i] >= _mse64(w, s) * (1 - 1e-4))
+
+
+def test_mse_levels_and_clamp(oracle_mod):
+    """Levels are clamp(rint(w / s), -7, 7) + 8 with the chosen fp32 step: checked in
+    exact arithmetic (ties excluded), including values beyond 7.5 steps that clamp."""
+    from fractions import Fraction
+    rng = np.random.default_rng(71)
+    W = (rng.standard_normal((16, 128)) * 0.02).astype(np.float32)
+    W[:, 0] = 0.3  # a large outlier per group: the search clamps it rather than widen the step
+    q, _, z, s32 = oracle_mod.quantize_pack_calibrated(W, "mse", 1000, with_fp32_scales=True)
+    lv = oracle_mod.unpack(q, 128).astype(np.int64) - 8
+    assert np.all(z == 8)
+    clamped = 0
+    for r in range(16):
+        s = Fraction(float(s32[r, 0]))
+        for k in range(128):
+            x = Fraction(float(W[r, k])) / s
+            fl = x.numerator // x.denominator
+            frac = x - fl
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 1 << 20):
+                continue
+            nearest = fl + (1 if frac > Fraction(1, 2) else 0)
+            exp = max(-7, min(7, nearest))
+            clamped += exp != nearest
+            assert lv[r, k] == exp
+    assert clamped > 0
