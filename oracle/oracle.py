@@ -70,6 +70,10 @@ def _load():
     lib.oracle_percentile_abs.restype = ctypes.c_float
     lib.oracle_mse_step.argtypes = [vp, ctypes.c_int, ctypes.c_int]
     lib.oracle_mse_step.restype = ctypes.c_float
+    lib.oracle_quantize_act_int8.argtypes = [vp, i64, i64, vp, vp]
+    lib.oracle_quantize_act_int8.restype = ctypes.c_int
+    lib.oracle_w4a8_matmul.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, dp, dp]
+    lib.oracle_w4a8_matmul.restype = ctypes.c_int
     lib.oracle_dequantize_16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, vp]
     lib.oracle_dequantize_16.restype = ctypes.c_int
     lib.oracle_f32_to_bf16_bits.argtypes = [ctypes.c_float]
@@ -241,6 +245,37 @@ def matmul(A_bf16: np.ndarray, qweight, scales, zeros):
     S = np.empty((M, N), np.float64)
     if _load().oracle_matmul(_ptr(A), M, N, K, _ptr(qweight), _ptr(s), _ptr(z), _ptr(Y), _ptr(S)):
         raise RuntimeError("oracle_matmul failed")
+    return Y, S
+
+
+def quantize_act_int8(A_bf16: np.ndarray):
+    """Per-token INT8 activations of A [M,K] (bf16 bit patterns): (a_q int8 [M,K],
+    s_a float32 [M]) with s_a = max(max|a|, 1e-8) / 127, a_q = clip(rint(a / s_a),
+    -128, 127), all in fp32."""
+    A = _as_u16_bits(A_bf16)
+    M, K = A.shape
+    aq = np.empty((M, K), np.int8)
+    sa = np.empty((M,), np.float32)
+    if _load().oracle_quantize_act_int8(_ptr(A), M, K, _ptr(aq), _ptr(sa)):
+        raise RuntimeError("oracle_quantize_act_int8 failed")
+    return aq, sa
+
+
+def w4a8_matmul(a_q: np.ndarray, a_scale: np.ndarray, qweight, scales, zeros):
+    """Y = (a_q * s_a) @ W_hat^T in float64, with S = sum_k |a_q s_a w_hat|: returns
+    (Y float64 [M,N], S float64 [M,N])."""
+    aq = np.ascontiguousarray(a_q, dtype=np.int8)
+    sa = np.ascontiguousarray(a_scale, dtype=np.float32)
+    M, K = aq.shape
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint8)
+    s = _as_u16_bits(scales)
+    z = np.ascontiguousarray(zeros, dtype=np.uint8)
+    N = qweight.shape[0]
+    Y = np.empty((M, N), np.float64)
+    S = np.empty((M, N), np.float64)
+    if _load().oracle_w4a8_matmul(_ptr(aq), _ptr(sa), M, N, K, _ptr(qweight), _ptr(s), _ptr(z),
+                                  _ptr(Y), _ptr(S)):
+        raise RuntimeError("oracle_w4a8_matmul failed")
     return Y, S
 
 

@@ -23,6 +23,10 @@
  *     values per byte, column 2j in the low nibble, 2j+1 in the high nibble) and
  *     "Step 5" (the dequantize-matmul y = x @ W_dequant^T, computed over chunks
  *     of output rows so only a chunk of W is ever dequantized at once).
+ *   - "Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with
+ *     Per-Channel Scale", "Step 3" (per-token INT8 activations: s_a = max|A| / 127
+ *     with max|A| clipped below at 1e-8, a_q = clip(round(A / s_a), -128, 127)) and
+ *     "Step 5" (forward_quant: a_q * s_a times the dequantized INT4 weights).
  *   The fixed convention on top of those pages: groups are 128 contiguous
  *   elements along K of W[N,K]; scale in fp32 (1 if max == min); IEEE fp32
  *   division; round half to even; scales stored as fp16, zero-points as uint8;
@@ -446,16 +450,15 @@ int oracle_dequantize_16(const uint8_t *qweight, const uint16_t *scales, const u
  * and S[m,n] = sum_k |A[m,k] * w_hat[n,k]| (the scale of the tolerance).
  * Follows the chunked dequantize-matmul pattern: dequantize a chunk of output rows,
  * then take the dot products against every activation row. */
-int oracle_matmul(const uint16_t *A, int64_t M, int64_t N, int64_t K,
-                  const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
-                  double *Y, double *S)
+/* Y = a * W_hat^T and S = sum |a * w_hat| in fp64 for activations already in fp64,
+ * over chunks of 256 output rows ([P4] Step 5's chunked dequantize-matmul). */
+static int matmul_f64(const double *a, int64_t M, int64_t N, int64_t K,
+                      const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                      double *Y, double *S)
 {
-    if (M < 0 || N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
     const int64_t chunk = 256;
-    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
     double *wc = (double *)malloc(sizeof(double) * (size_t)(chunk * K > 0 ? chunk * K : 1));
-    if (!a || !wc) { free(a); free(wc); return -2; }
-    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_bf16_to_f64(A[i]);
+    if (!wc) return -2;
     for (int64_t n0 = 0; n0 < N; n0 += chunk) {
         int64_t rows = (N - n0 < chunk) ? N - n0 : chunk;
         dequant_rows(qweight, scales, zeros, n0, rows, K, wc);
@@ -472,9 +475,66 @@ int oracle_matmul(const uint16_t *A, int64_t M, int64_t N, int64_t K,
             }
         }
     }
-    free(a);
     free(wc);
     return 0;
+}
+
+int oracle_matmul(const uint16_t *A, int64_t M, int64_t N, int64_t K,
+                  const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                  double *Y, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    if (!a) return -2;
+    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_bf16_to_f64(A[i]);
+    int rc = matmul_f64(a, M, N, K, qweight, scales, zeros, Y, S);
+    free(a);
+    return rc;
+}
+
+/* ---- W4A8: per-token INT8 dynamic activation quantization -------------------------
+ * "Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with Per-Channel
+ * Scale", Step 3 (activations_to_int8): per token (row of A), in fp32,
+ *     s_a = max(max_k |a|, 1e-8) / 127,   a_q = clip(round_half_even(a / s_a), -128, 127).
+ * A arrives as bf16 (the library's activation type) and widens exactly to fp32. */
+int oracle_quantize_act_int8(const uint16_t *A, int64_t M, int64_t K, int8_t *a_q, float *a_scale)
+{
+    if (M < 0 || K < 0) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = fabsf((float)oracle_bf16_to_f64(A[m * K + k]));
+            if (v > amax) amax = v;
+        }
+        float s = fmaxf(amax, 1e-8f) / 127.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = (float)oracle_bf16_to_f64(A[m * K + k]);
+            float t = rintf(v / s);
+            t = fminf(fmaxf(t, -128.0f), 127.0f);
+            a_q[m * K + k] = (int8_t)(int)t;
+        }
+        a_scale[m] = s;
+    }
+    return 0;
+}
+
+/* The W4A8 product (Step 5, forward_quant: the INT8 activations times their per-token
+ * scale, multiplied by the dequantized INT4 weights), in fp64:
+ *     Y[m,n] = sum_k (a_q[m,k] * s_a[m]) * w_hat[n,k],  S = sum_k |...|.
+ * Every product is exact in fp64 (8 + 24 + 4 + 11 significant bits). */
+int oracle_w4a8_matmul(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N, int64_t K,
+                       const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                       double *Y, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    if (!a) return -2;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            a[m * K + k] = (double)a_q[m * K + k] * (double)a_scale[m];
+    int rc = matmul_f64(a, M, N, K, qweight, scales, zeros, Y, S);
+    free(a);
+    return rc;
 }
 
 /* The same quantity for a list of (m, n) output positions, one by one; used to

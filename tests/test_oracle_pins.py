@@ -517,3 +517,93 @@ def test_mse_levels_and_clamp(oracle_mod):
             clamped += exp != nearest
             assert lv[r, k] == exp
     assert clamped > 0
+
+
+# ---- W4A8 ("Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with
+# Per-Channel Scale", Step 3 and Step 5) ----------------------------------------------------
+def _bf16(x):
+    import synth
+    return synth.f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def test_act_int8_hand_rows(oracle_mod):
+    """Hand-worked rows.  amax = 127 gives s_a = 1, so a_q = rint(a) with ties to even:
+    2.5 -> 2, -3.5 -> -4, 0.5 -> 0, 1.5 -> 2.  amax = 254 gives s_a = 2: 1 / 2 = 0.5 -> 0,
+    3 / 2 = 1.5 -> 2, 5 / 2 = 2.5 -> 2.  An all-zero row takes s_a = fl(1e-8) / 127 and
+    a_q = 0.  amax = 1: s_a = fl(1/127), and the extreme elements land on +-127."""
+    rows = np.zeros((4, 128), np.float32)
+    rows[0, :7] = [127, 2.5, -3.5, 0.5, -0.5, 1.5, -127]
+    rows[1, :5] = [254, 1, 3, 5, -254]
+    rows[3, :3] = [1.0, -1.0, 0.25]
+    aq, sa = oracle_mod.quantize_act_int8(_bf16(rows))
+    assert list(aq[0, :7]) == [127, 2, -4, 0, 0, 2, -127] and np.all(aq[0, 7:] == 0)
+    assert list(aq[1, :5]) == [127, 0, 2, 2, -127]
+    assert sa[0] == 1.0 and sa[1] == 2.0
+    assert sa[2] == np.float32(1e-8) / np.float32(127) and np.all(aq[2] == 0)
+    assert sa[3] == np.float32(1.0) / np.float32(127.0)
+    assert aq[3, 0] == 127 and aq[3, 1] == -127 and aq[3, 2] == 32   # 0.25 * 127 = 31.75 -> 32
+
+
+def test_act_int8_exact_rounding_and_bounds(oracle_mod):
+    """Each level is the nearest integer to a / s_a in exact arithmetic (ties excluded),
+    |a_q| <= 127, the row's largest magnitude maps to +-127, and |a - a_q s_a| <= s_a / 2."""
+    from fractions import Fraction
+    import synth
+    rng = np.random.default_rng(91)
+    A = synth.f32_to_bf16_bits((rng.standard_normal((6, 384)) * 10.0 ** rng.integers(-3, 3, (6, 1)))
+                               .astype(np.float32))
+    aq, sa = oracle_mod.quantize_act_int8(A)
+    a = oracle_mod.bf16_bits_to_f64(A)
+    assert np.all(np.abs(aq.astype(int)) <= 127)
+    for m in range(6):
+        s = Fraction(float(sa[m]))
+        assert abs(aq[m, np.argmax(np.abs(a[m]))]) == 127
+        for k in range(384):
+            x = Fraction(float(a[m, k])) / s
+            fl = x.numerator // x.denominator
+            frac = x - fl
+            # the fp32 quotient is within half an ulp (2^-24 |x|) of x: skip near-ties
+            if abs(frac - Fraction(1, 2)) <= abs(x) / (1 << 22) + Fraction(1, 1 << 40):
+                continue
+            assert aq[m, k] == fl + (1 if frac > Fraction(1, 2) else 0)
+        # near a tie the fp32 quotient (within 127.5 * 2^-24 of a / s_a) may round to the
+        # farther integer: |a / s_a - a_q| <= 1/2 + 2^-17
+        assert np.all(np.abs(a[m] - aq[m] * float(sa[m])) <= float(sa[m]) / 2 * (1 + 2.0 ** -15))
+
+
+def test_w4a8_matmul_integer_special_case(oracle_mod):
+    """Integer weights (a group spanning [0, 15] exactly: s = 1, zp = 0) and s_a = 1
+    (a row whose largest magnitude is 127): Y is the integer product a_q q, exact."""
+    rng = np.random.default_rng(92)
+    N, K, M = 20, 256, 3
+    W = rng.integers(0, 16, (N, K)).astype(np.float16)
+    W[:, ::128] = 0
+    W[:, 1::128] = 15
+    q, s, z = oracle_mod.quantize_pack(W)
+    assert np.all(z == 0) and np.all(s == 1)
+    A = rng.integers(-127, 128, (M, K)).astype(np.float32)
+    A[:, 0] = 127
+    aq, sa = oracle_mod.quantize_act_int8(_bf16(A))
+    assert np.all(sa == 1) and np.array_equal(aq.astype(np.float32), A)
+    Y, S = oracle_mod.w4a8_matmul(aq, sa, q, s, z)
+    qi = oracle_mod.unpack(q, K).astype(np.int64)
+    assert np.array_equal(Y, (aq.astype(np.int64) @ qi.T).astype(np.float64))
+    assert np.array_equal(S, (np.abs(aq.astype(np.int64)) @ qi.T).astype(np.float64))
+
+
+def test_w4a8_matmul_equals_w4a16_on_representable_activations(oracle_mod):
+    """With s_a a power of two (largest magnitude 127 * 2^e), a_q * s_a is an exact bf16
+    value, so the W4A8 product equals the pinned W4A16 product on those activations."""
+    import synth
+    W, _ = synth.make_random(70, 512, 1, seed=93)
+    q, s, z = oracle_mod.quantize_pack(W)
+    rng = np.random.default_rng(93)
+    A = rng.standard_normal((4, 512)).astype(np.float32)
+    A[:, 7] = 127 * np.float32(2.0) ** np.arange(-6, -2)       # row maxima 127 * 2^e
+    A = np.clip(A, -A[:, 7:8], A[:, 7:8])
+    aq, sa = oracle_mod.quantize_act_int8(_bf16(A))
+    assert np.array_equal(sa, np.float32(2.0) ** np.arange(-6, -2))
+    A2 = _bf16(aq.astype(np.float32) * sa[:, None])
+    Y1, S1 = oracle_mod.w4a8_matmul(aq, sa, q, s, z)
+    Y2, S2 = oracle_mod.matmul(A2, q, s, z)
+    assert np.array_equal(Y1, Y2) and np.array_equal(S1, S2)
