@@ -196,6 +196,20 @@ def test_matmul_streaming_gemv(env, M, N, K):
     assert_matmul_ok(env, A, q, s, z)
 
 
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 12, 16])
+@pytest.mark.parametrize("N,K", [(1, 2048), (15, 2048), (17, 4096), (300, 8192), (1031, 2048),
+                                 (9, 6144), (2500, 4096)])
+def test_matmul_decode_mma(env, M, N, K):
+    """The warp-MMA decode kernel (1 <= M <= 16, K a multiple of 2048): one or two
+    8-column activation blocks, N tails inside a 16-row tile, CTAs with one or many
+    tiles, one to four 2048-wide stages per tile."""
+    import synth
+    _, _, orc = env
+    W, A = synth.make_random(N, K, M, seed=31 * N + K + M)
+    q, s, z = orc.quantize_pack(W)
+    assert_matmul_ok(env, A, q, s, z)
+
+
 @pytest.mark.parametrize("M", [1, 2, 3, 8])
 def test_matmul_streaming_zero_rows(env, M):
     """Rows of W that are all zero reconstruct to 0 exactly, so those outputs must be
