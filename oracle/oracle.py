@@ -74,6 +74,8 @@ def _load():
     lib.oracle_quantize_act_int8.restype = ctypes.c_int
     lib.oracle_w4a8_matmul.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, dp, dp]
     lib.oracle_w4a8_matmul.restype = ctypes.c_int
+    lib.oracle_gptq_quantize.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
+    lib.oracle_gptq_quantize.restype = ctypes.c_int
     lib.oracle_dequantize_16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, vp]
     lib.oracle_dequantize_16.restype = ctypes.c_int
     lib.oracle_f32_to_bf16_bits.argtypes = [ctypes.c_float]
@@ -182,6 +184,43 @@ def mse_step(group: np.ndarray, n: int) -> np.float32:
     """The MSE calibrator's chosen step for one group (fp32 values)."""
     g = np.ascontiguousarray(group, dtype=np.float32)
     return np.float32(_load().oracle_mse_step(_ptr(g), len(g), int(n)))
+
+
+def gptq_factor(X: np.ndarray, damp: float = 1e-4) -> np.ndarray:
+    """The upper Cholesky factor U of H^-1 (H^-1 = U^T U) from calibration activations
+    X [n, K], with H = X^T X / n + damp * mean(diag(H)) * I ("Build a GPTQ INT4
+    Quantization Engine in Python/NumPy", Step 3, compute_hessian), computed in fp64
+    with numpy's inverse and Cholesky and returned as fp32 (the quantizer's input)."""
+    X = np.asarray(X, np.float64)
+    H = X.T @ X / X.shape[0]
+    H += damp * np.mean(np.diag(H)) * np.eye(H.shape[0])
+    Hinv = np.linalg.inv(H)
+    L = np.linalg.cholesky(Hinv)          # Hinv = L L^T, L lower
+    return np.ascontiguousarray(L.T, dtype=np.float32)
+
+
+def gptq_quantize(W: np.ndarray, U: np.ndarray):
+    """GPTQ quantization of W[N,K] (float16 or float32) given U (fp32 [K,K]): returns
+    (qweight, scales float16, zeros) in the layout of quantize_pack."""
+    N, K = W.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    if W.dtype == np.float16:
+        src, dt = _as_u16_bits(W), 0
+    elif W.dtype == np.float32:
+        src, dt = np.ascontiguousarray(W), 1
+    else:
+        raise TypeError("W must be float16 or float32")
+    U = np.ascontiguousarray(U, dtype=np.float32)
+    if U.shape != (K, K):
+        raise ValueError("U must be [K, K]")
+    ng = K // GROUP
+    q = np.empty((N, K // 2), np.uint8)
+    s = np.empty((N, ng), np.uint16)
+    z = np.empty((N, ng), np.uint8)
+    if _load().oracle_gptq_quantize(_ptr(src), dt, N, K, _ptr(U), _ptr(q), _ptr(s), _ptr(z)):
+        raise RuntimeError("oracle_gptq_quantize failed")
+    return q, s.view(np.float16), z
 
 
 def unpack(qweight: np.ndarray, K: int) -> np.ndarray:

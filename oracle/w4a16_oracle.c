@@ -23,6 +23,10 @@
  *     values per byte, column 2j in the low nibble, 2j+1 in the high nibble) and
  *     "Step 5" (the dequantize-matmul y = x @ W_dequant^T, computed over chunks
  *     of output rows so only a chunk of W is ever dequantized at once).
+ *   - "Build a GPTQ INT4 Quantization Engine in Python/NumPy", "Step 3" (GPTQ:
+ *     the columns are quantized left to right and each column's quantization
+ *     error, divided by the diagonal of the Cholesky factor of H^-1, is fed into
+ *     the columns not yet quantized).
  *   - "Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with
  *     Per-Channel Scale", "Step 3" (per-token INT8 activations: s_a = max|A| / 127
  *     with max|A| clipped below at 1e-8, a_q = clip(round(A / s_a), -128, 127)) and
@@ -374,6 +378,63 @@ int oracle_quantize_pack_calib(const void *W, int w_dtype, int64_t N, int64_t K,
     if (method == 3 && !(param >= 1.0)) return -1;
     if (method != 2 && method != 3) return -1;
     return quantize_pack_mode(W, w_dtype, N, K, method, param, qweight, scales, zeros, scales32);
+}
+
+/* ---- GPTQ: second-order column-greedy quantization ------------------------------
+ * "Build a GPTQ INT4 Quantization Engine in Python/NumPy", Step 3.  The page's listing
+ * sweeps output rows with a K x K factor indexed by rows; the algorithm it names (and
+ * follows in prose) sweeps the input columns, which is what is done here, row by row
+ * (rows are independent):
+ *   U = the upper-triangular Cholesky factor of H^-1 (H^-1 = U^T U), given as fp32 [K,K]
+ *       (computed by the caller from the calibration activations).
+ *   w = the row, widened exactly to fp32.  For j = 0 .. K-1:
+ *     at a group start (j % 128 == 0): the group's s and zp from the current values
+ *       w[j .. j+127] by the rule of w4_quantize_pack (fp32 min/max, s = (max-min)/15
+ *       or 1, zp = clip(rint(-min/s), 0, 15)), s16 = fp16(s);
+ *     q_j = clip(rint(w_j / s) + zp, 0, 15);
+ *     e   = (w_j - (q_j - zp) * s16) / U[j][j]        (the reconstruction inference uses)
+ *     w_c = fmaf(-e, U[j][c], w_c) for c = j+1 .. K-1, in that order.
+ * Every operation is IEEE fp32 with round-to-nearest-even (fmaf fused).  Outputs in
+ * the layout of oracle_quantize_pack. */
+int oracle_gptq_quantize(const void *W, int w_dtype, int64_t N, int64_t K, const float *U,
+                         uint8_t *qweight, uint16_t *scales, uint8_t *zeros)
+{
+    if (N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    if (w_dtype != 0 && w_dtype != 1) return -1;
+    const int64_t ng = K / ORACLE_GROUP;
+    float *w = (float *)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1));
+    uint8_t *q = (uint8_t *)malloc((size_t)(K > 0 ? K : 1));
+    if (!w || !q) { free(w); free(q); return -2; }
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k)
+            w[k] = (w_dtype == 0) ? oracle_f16_to_f32(((const uint16_t *)W)[n * K + k])
+                                  : ((const float *)W)[n * K + k];
+        float s = 1.0f, s16f = 1.0f;
+        int zp = 0;
+        for (int64_t j = 0; j < K; ++j) {
+            if (j % ORACLE_GROUP == 0) {
+                uint8_t scratch[ORACLE_GROUP];
+                quantize_group(w + j, ORACLE_GROUP, scratch, &s, &zp);
+                uint16_t sb = oracle_f32_to_f16_bits(s);
+                s16f = oracle_f16_to_f32(sb);
+                scales[n * ng + j / ORACLE_GROUP] = sb;
+                zeros[n * ng + j / ORACLE_GROUP] = (uint8_t)zp;
+            }
+            float t = rintf(w[j] / s) + (float)zp;
+            float c = fminf(fmaxf(t, 0.0f), 15.0f);
+            q[j] = (uint8_t)(int)c;
+            float rec = (float)((int)q[j] - zp) * s16f;
+            float d = w[j] - rec;
+            float e = d / U[j * K + j];
+            for (int64_t cc = j + 1; cc < K; ++cc)
+                w[cc] = fmaf(-e, U[j * K + cc], w[cc]);
+        }
+        for (int64_t jb = 0; jb < K / 2; ++jb)
+            qweight[n * (K / 2) + jb] = (uint8_t)(q[2 * jb] | (q[2 * jb + 1] << 4));
+    }
+    free(w);
+    free(q);
+    return 0;
 }
 
 /* Unpack qweight[N,K/2] into q[N,K] (one value 0..15 per byte). */

@@ -607,3 +607,67 @@ def test_w4a8_matmul_equals_w4a16_on_representable_activations(oracle_mod):
     Y1, S1 = oracle_mod.w4a8_matmul(aq, sa, q, s, z)
     Y2, S2 = oracle_mod.matmul(A2, q, s, z)
     assert np.array_equal(Y1, Y2) and np.array_equal(S1, S2)
+
+
+# ---- GPTQ ("Build a GPTQ INT4 Quantization Engine in Python/NumPy", Step 3) -------------
+def test_gptq_hand_worked_feed(oracle_mod):
+    case = parse_cases(os.path.join(GOLDEN_DIR, "gptq_cases.txt"))[0]
+    K = 128
+    U = np.eye(K, dtype=np.float32)
+    U[0, 0], U[0, 1] = 2.0, -4.0
+    w = np.zeros((1, K), np.float32)
+    w[0, :4] = [0.5625, 1.25, -1.5, 2.25]
+    q, s, z = oracle_mod.gptq_quantize(w, U)
+    lv = oracle_mod.unpack(q, K)[0]
+    exp = [int(x) for x in case["levels"].split()]
+    assert list(lv[:4]) == exp and np.all(lv[4:] == int(case["rest"]))
+    assert s[0, 0] == np.float16(float(case["scale"])) and z[0, 0] == int(case["zero"])
+    q_rtn = oracle_mod.unpack(oracle_mod.quantize_pack(w)[0], K)[0]
+    assert q_rtn[1] == 11 and lv[1] == 12          # the fed-forward error changed the level
+
+
+@pytest.mark.parametrize("diag", [False, True])
+def test_gptq_without_correlation_is_round_to_nearest(oracle_mod, diag):
+    """With U diagonal (uncorrelated inputs) every fed-forward term is exactly zero, so
+    GPTQ reduces to the pinned round-to-nearest quantizer."""
+    import synth
+    W, _ = synth.make_random(48, 512, 1, seed=95)
+    U = np.eye(512, dtype=np.float32)
+    if diag:
+        U *= np.random.default_rng(95).uniform(0.5, 3.0, 512).astype(np.float32)
+    for a, b in zip(oracle_mod.gptq_quantize(W, U), oracle_mod.quantize_pack(W)):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+def test_gptq_reduces_the_layer_error(oracle_mod):
+    """GPTQ minimizes the layer-output error greedily: on correlated calibration inputs
+    its H-weighted reconstruction error tr((W - W_hat) H (W - W_hat)^T) is well below
+    round-to-nearest's, row by row.  A sign error or a transposed U in the update
+    would raise it instead."""
+    import synth
+    rng = np.random.default_rng(96)
+    K = 512
+    X = rng.standard_normal((4096, K))
+    X[:, 1:] += 0.9 * X[:, :-1]
+    U = oracle_mod.gptq_factor(X)
+    assert np.allclose(np.triu(U), U)
+    W, _ = synth.make_random(64, K, 1, seed=96)
+    H = X.T @ X / X.shape[0]
+
+    def loss(q, s, z):
+        D = W.astype(np.float64) - oracle_mod.dequantize(q, s, z, K)
+        return np.einsum("nk,kl,nl->n", D, H, D)
+
+    lg, lr = loss(*oracle_mod.gptq_quantize(W, U)), loss(*oracle_mod.quantize_pack(W))
+    assert lg.mean() < 0.8 * lr.mean()
+    assert np.mean(lg < lr) > 0.9
+
+
+def test_gptq_factor_inverts_the_hessian(oracle_mod):
+    """U^T U = H^-1 for the damped Hessian (checked in fp64 against numpy's inverse)."""
+    rng = np.random.default_rng(97)
+    X = rng.standard_normal((1000, 256))
+    U = oracle_mod.gptq_factor(X).astype(np.float64)
+    H = X.T @ X / 1000
+    H += 1e-4 * np.mean(np.diag(H)) * np.eye(256)
+    assert np.allclose(U.T @ U @ H, np.eye(256), atol=1e-4)
