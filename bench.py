@@ -60,6 +60,9 @@ OTHER_WORKLOADS = ["llama7b_gemv", "skinny_m8", "prefill_gemm"]
 ROTATE_L2 = 3              # rotating input copies span >= 3x the L2 size
 MAX_COPIES = 64            # cap for tiny inputs (the correctness-only configuration)
 MAX_GRAPH = 1000           # launches per captured CUDA graph at most
+MSE_LAUNCHES = 5           # the MSE-search calibrator (~30 ms a launch) is timed over this many
+GPTQ_LAUNCHES = 3          # GPTQ (O(N K^2) fused multiply-adds, ms a launch) likewise
+GPTQ_WORKLOAD = "llama7b_gemv"
 SLEEP_CYCLES = 4_000_000   # ~2 ms sleep kernel ahead of each event window
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -68,6 +71,9 @@ KERNEL_SOURCES = {  # every file a kernel is compiled from (its digest dates a p
     "quantize_pack": [CSRC + "quantize_pack.cuh", CSRC + "common.cuh"],
     "gemv": [CSRC + "gemv_dp4a.cuh", CSRC + "gemv.cuh", CSRC + "common.cuh"],
     "gemv_mma": [CSRC + "gemv_mma.cuh", CSRC + "common.cuh"],
+    "quantize_calib": [CSRC + "quantize_calib.cuh", CSRC + "common.cuh"],
+    "act_quant": [CSRC + "act_quant.cuh", CSRC + "common.cuh"],
+    "gptq": [CSRC + "gptq.cuh", CSRC + "common.cuh"],
     "gemm_tcgen05": [CSRC + "gemm_tcgen05.cuh", CSRC + "common.cuh"],
     "dequantize": [CSRC + "dequantize.cuh", CSRC + "common.cuh"],
 }
@@ -119,6 +125,8 @@ def measured_peaks():
 
 def matmul_kernel_name(M: int, K: int) -> str:
     """Which kernel family w4_matmul runs for this shape (mirrors the dispatch)."""
+    if 2 <= M <= 16 and K % 2048 == 0 and M * K * 2 <= 128 * 1024:
+        return "gemv_mma"
     if M > 8:
         return "gemm_tcgen05"
     return "gemv"
@@ -461,6 +469,62 @@ def run_workload(w4, torch, np, synth, timer, wl_name, steps, warmup, l2, peaks,
                                           rotation=f"{cm} packed copies, {co} output copies",
                                           traffic=profiled_traffic("dequantize", wl_name))
         del outs
+        # Clip-range calibration: the percentile calibrator over K launches; the MSE
+        # search (1000 candidates, n * 128 divisions per group: arithmetic-bound) over
+        # MSE_LAUNCHES launches on the first rows that make ~1/8 of the matrix.
+        pc_s, _ = timer.time(lambda i, s_: w4.quantize_pack(
+            Wds[i % cw], out=(qs[i % cm], ss[i % cm], zs[i % cm]), stream=s_, calibration="percentile", param=99.9),
+            steps, warmup, period)
+        ks["quantize_pack_percentile"] = hbm_entry(pc_s, qb, peaks, launches=steps, p=99.9,
+                                                   groups_per_s=N * K / 128 / pc_s)
+        rows = max(1, N // 8)
+        Wsub = [w[:rows] for w in Wds]
+        outs_sub = [(q[:rows], s[:rows], z[:rows]) for q, s, z in zip(qs, ss, zs)]
+        n_mse = min(steps, MSE_LAUNCHES)
+        mse_s, _ = timer.time(lambda i, s_: w4.quantize_pack(
+            Wsub[i % cw], out=outs_sub[i % cm], stream=s_, calibration="mse", param=1000),
+            n_mse, 1, period)
+        ks["quantize_pack_mse"] = {"us": mse_s * 1e6, "rows": rows, "candidates": 1000, "launches": n_mse,
+                                   "groups_per_s": rows * K / 128 / mse_s,
+                                   "GB/s": quantize_bytes(rows, K, W.dtype.itemsize) / mse_s / 1e9,
+                                   "bound": "alu (1000 candidates x 128 divisions per group)"}
+    if extras and wl_name == GPTQ_WORKLOAD:
+        # GPTQ on synthetic calibration activations X [2K, K] ~ N(0, 1) with neighbouring
+        # inputs correlated (x_k += 0.9 x_(k-1)); the kernel's input U, the upper Cholesky
+        # factor of the damped H^-1, is prepared on the host with numpy in fp64.
+        rng = np.random.default_rng(11)
+        X = rng.standard_normal((2 * K, K))
+        X[:, 1:] += 0.9 * X[:, :-1]
+        H = X.T @ X / X.shape[0]
+        H += 1e-4 * np.mean(np.diag(H)) * np.eye(K)
+        U = np.ascontiguousarray(np.linalg.cholesky(np.linalg.inv(H)).T, dtype=np.float32)
+        Ud = torch.from_numpy(U).to(dev)
+        del X, H, U
+        n_g = min(steps, GPTQ_LAUNCHES)
+        g_s, _ = timer.time(lambda i, s_: w4.gptq_quantize(Wds[i % cw], Ud, out=(qs[i % cm], ss[i % cm], zs[i % cm]),
+                                                           stream=s_), n_g, 1, period)
+        ks["gptq_quantize"] = {"us": g_s * 1e6, "launches": n_g, "fma": N * K * (K - 1) // 2,
+                               "TFMA/s": N * K * (K - 1) / 2 / g_s / 1e12,
+                               "bound": "fp32 fused multiply-adds (O(N K^2), sequential per element)"}
+        del Ud
+    if extras:
+        # W4A8: the per-token INT8 activation quantizer, then the W4A8 matmul on the same
+        # packed copies (the GEMM path widens a_q into a workspace; the decode path needs none).
+        aq, sa = w4.quantize_act_int8(Ad)
+        actq_s, _ = timer.time(lambda i, s_: w4.quantize_act_int8(Ad, stream=s_, out=(aq, sa)), steps, warmup, 1)
+        need = w4.w4_matmul_w4a8_workspace_size(M, K)
+        ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+        w8_s, w8_graph = timer.time(lambda i, s_: w4.matmul_w4a8(
+            aq, sa, qs[i % cm], ss[i % cm], zs[i % cm], out=Y, stream=s_, workspace=ws), steps, warmup, cm)
+        ks["quantize_act_int8"] = hbm_entry(actq_s, 3 * M * K + 4 * M, peaks, launches=steps,
+                                            note="A is read twice and may stay in L2 between launches")
+        fl = matmul_flops(M, N, K)
+        w8b = N * K // 2 + 3 * N * (K // 128) + M * K + 4 * M + 2 * M * N
+        ent = hbm_entry(w8_s, w8b, peaks, launches=steps, workspace_bytes=need, graphs=w8_graph)
+        ent["TFLOP/s"] = fl / w8_s / 1e12
+        ent["frac_bf16_burst"] = ent["TFLOP/s"] / peaks["bf16_tflops"]
+        ks["matmul_w4a8"] = ent
+        del ws
     del Wds, qs, ss, zs, Y, Ad
     torch.cuda.empty_cache()
     return ks, (q_s, m_s), info
@@ -595,6 +659,58 @@ def run_ours(args, ws, rank, local, dist):
     return result
 
 
+# ---- one launch of one kernel (for profiler captures) ------------------------------------
+ONCE_KERNELS = ("quantize_pack", "quantize_pack_sym", "quantize_pack_percentile", "quantize_pack_mse",
+                "dequantize", "matmul", "quantize_act_int8", "matmul_w4a8", "gptq_quantize")
+
+
+def run_once(args):
+    """Two launches of one kernel on the workload's inputs (the first warms up), then a
+    device sync: a small, self-contained command for profiler captures.  No timing."""
+    import numpy as np
+    import torch
+    import synth
+    import w4a16_matmul_asym_b300 as w4
+    dev = torch.device("cuda", 0)
+    W, A = synth.make_workload(args.workload)
+    M, N, K = A.shape[0], W.shape[0], W.shape[1]
+    Wd = torch.from_numpy(W).to(dev)
+    Ad = torch.from_numpy(A.view(np.int16)).to(dev).view(torch.bfloat16)
+    q, s, z = w4.quantize_pack(Wd)
+    name = args.once
+    if name == "gptq_quantize":
+        rng = np.random.default_rng(11)
+        X = rng.standard_normal((2 * K, K))
+        X[:, 1:] += 0.9 * X[:, :-1]
+        H = X.T @ X / X.shape[0]
+        H += 1e-4 * np.mean(np.diag(H)) * np.eye(K)
+        Ud = torch.from_numpy(np.ascontiguousarray(np.linalg.cholesky(np.linalg.inv(H)).T, dtype=np.float32)).to(dev)
+    aq, sa = w4.quantize_act_int8(Ad)
+    for _ in range(2):
+        if name == "quantize_pack":
+            w4.quantize_pack(Wd, out=(q, s, z))
+        elif name == "quantize_pack_sym":
+            w4.quantize_pack(Wd, out=(q, s, z), symmetric=True)
+        elif name == "quantize_pack_percentile":
+            w4.quantize_pack(Wd, out=(q, s, z), calibration="percentile", param=99.9)
+        elif name == "quantize_pack_mse":
+            w4.quantize_pack(Wd[: max(1, N // 8)], calibration="mse", param=1000)
+        elif name == "dequantize":
+            w4.dequantize(q, s, z)
+        elif name == "matmul":
+            w4.matmul(Ad, q, s, z)
+        elif name == "quantize_act_int8":
+            w4.quantize_act_int8(Ad, out=(aq, sa))
+        elif name == "matmul_w4a8":
+            w4.matmul_w4a8(aq, sa, q, s, z)
+        elif name == "gptq_quantize":
+            w4.gptq_quantize(Wd, Ud, out=(q, s, z))
+    torch.cuda.synchronize(dev)
+    rc = w4.w4_check_device_error(0)
+    print(json.dumps({"once": name, "workload": args.workload, "M": M, "N": N, "K": K, "status": rc}))
+    return 0 if rc == 0 else 1
+
+
 # ---- reference arm: the CPU oracle alone ------------------------------------------------
 def run_reference(args, ws, rank):
     import synth
@@ -650,11 +766,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="time the step workload only (no other workloads or extra kernels)")
+    ap.add_argument("--once", choices=ONCE_KERNELS,
+                    help="run one kernel twice on the workload and exit (for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
+    if args.once:
+        return run_once(args)
     ws, rank, local = dist_info()
     if args.impl == "reference":
         if rank == 0:

@@ -13,8 +13,9 @@
  *                                      rounded to nearest-even bf16
  * Groups are 128 contiguous elements along K of one row of W.
  *
- * Ownership: the caller allocates and owns every buffer; the library allocates no
- * device or host memory, keeps no per-call state, and holds no pointer after return.
+ * Ownership: the caller allocates and owns every buffer (including the scratch
+ * workspace w4_matmul_w4a8 may ask for); the library allocates no device or host
+ * memory, keeps no per-call state, and holds no pointer after return.
  * Asynchrony: every call enqueues work on the caller's stream and returns without
  * synchronizing.  On a validation failure a call returns before launching anything
  * and leaves every output untouched.
@@ -109,6 +110,74 @@ W4_API int w4_quantize_pack_sym(const void *W, int w_dtype, int64_t N, int64_t K
                                 uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream);
 
 /*
+ * w4_quantize_pack_percentile / w4_quantize_pack_mse -- symmetric quantization with a
+ * calibrated clip range per group of 128 elements along K, in the layout of
+ * w4_quantize_pack (every zero point 8), so that w4_matmul and w4_dequantize consume
+ * the result unchanged.
+ *
+ * Defined by: "Building a From-Scratch Group-Wise INT4 Quantization Layer for LLaMA
+ * Weights" (Step 4, ScaleCalibrator: the percentile of |w| as the clip range, and the
+ * search over linspace(min|w|, max|w|, n) candidate steps minimizing the reconstruction
+ * MSE with levels round(w / s).clamp(-7, 7)).  Exact convention, per group, values
+ * widened exactly to fp32, every operation IEEE fp32 with round-to-nearest-even:
+ *   percentile (0 < p <= 100): sort |w| ascending (a_0 .. a_127); h = (p / 100) * 127,
+ *     lo = floor(h), f = h - lo, r = a_lo + f * (a_min(lo+1,127) - a_lo);
+ *     s = (r == 0) ? 1 : r / 7.
+ *   mse (candidates = n >= 1): c_i = min|w| + i * ((max|w| - min|w|) / (n - 1)) for
+ *     i < n - 1, c_(n-1) = max|w| (n == 1: c_0 = min|w|); skip c_i < 1e-10; score(c) =
+ *     (sum over k = 0..127 in order of d_k * d_k) / 128 with d_k = clamp(rint(w_k / c),
+ *     -7, 7) * c - w_k; s = the first c_i with the smallest score (1e-8 if none).
+ *   level = clamp(round_half_even(w / s), -7, 7) + 8, zeros = 8,
+ *   scales = fp16_round_nearest_even(s).
+ * Bit-exact with that definition for finite inputs (for mse: |w| small enough that the
+ * squared errors stay finite in fp32, e.g. any fp16 input).  The mse search performs
+ * n * 128 divisions per group: an offline calibration step, bound by arithmetic.
+ *
+ * Arguments, alignment, empty problems and errors: as w4_quantize_pack; p outside
+ * (0, 100] or candidates outside [1, 2^24] give W4_ERR_INVALID_ARG.
+ */
+W4_API int w4_quantize_pack_percentile(const void *W, int w_dtype, int64_t N, int64_t K, int group,
+                                       float p, uint8_t *qweight, void *scales, uint8_t *zeros,
+                                       cudaStream_t stream);
+W4_API int w4_quantize_pack_mse(const void *W, int w_dtype, int64_t N, int64_t K, int group,
+                                int candidates, uint8_t *qweight, void *scales, uint8_t *zeros,
+                                cudaStream_t stream);
+
+/*
+ * w4_gptq_quantize -- GPTQ: quantize W[N,K] into the layout of w4_quantize_pack (4-bit
+ * levels, fp16 scales, uint8 zero points per group of 128 along K), column by column,
+ * feeding each column's quantization error into the columns not yet quantized.
+ *
+ * Defined by: "Build a GPTQ INT4 Quantization Engine in Python/NumPy" (Step 3: the
+ * Hessian of the calibration activations, the Cholesky factor of its inverse, and the
+ * column-greedy quantization with error propagation).  Exact convention, per row, values
+ * widened exactly to fp32, every step an IEEE fp32 operation (fused multiply-add for
+ * the updates):
+ *   for j = 0 .. K-1:
+ *     if j % 128 == 0: s, zp of the current w[j .. j+127] by the rule of
+ *       w4_quantize_pack; scales = s16 = fp16_round_nearest_even(s), zeros = zp;
+ *     q_j = clip(round_half_even(w_j / s) + zp, 0, 15);
+ *     e   = (w_j - (q_j - zp) * s16) / U[j][j];
+ *     w_c = fma(-e, U[j][c], w_c) for every c > j (each w_c updated in ascending j).
+ * Bit-exact with that definition.  U is the caller's: the upper-triangular Cholesky
+ * factor of H^-1 (H^-1 = U^T U, H the damped Hessian X^T X / n + damp I of the
+ * calibration activations X), fp32 [K, K] row-major; only its upper triangle is read
+ * and its diagonal must be nonzero.
+ *
+ * Arguments:
+ *   W        device pointer, fp16 or fp32 [N, K] per w_dtype; 16-byte aligned.
+ *   N, K     N >= 0, K >= 0, K % group == 0; K <= 8192 (W4_ERR_UNSUPPORTED above).
+ *   group    must be 128.
+ *   U        device pointer, fp32 [K, K]; 16-byte aligned.
+ *   qweight, scales, zeros  outputs as in w4_quantize_pack.
+ *   stream   the stream to run on.
+ * N == 0 or K == 0: W4_OK, nothing launched.  The work is O(N K^2) fused multiply-adds
+ * (an offline step, bound by the FMA rate).
+ */
+W4_API int w4_gptq_quantize(const void *W, int w_dtype, int64_t N, int64_t K, int group, const float *U,
+                            uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream);
+
+/*
  * w4_dequantize -- materialize W_hat[N,K] = (q - zp) * scale_fp16 as a 16-bit tensor,
  * the explicit dequantize path for a consumer that wants the whole weight matrix.
  *
@@ -143,12 +212,13 @@ W4_API int w4_dequantize(const uint8_t *qweight, const void *scales, const uint8
  * path).  Accuracy contract, per output element:
  *     |Y - Y_exact| <= 8e-3 * sum_k |A[m,k] * W_hat[n,k]| + ulp_bf16(|Y_exact|) / 2.
  * Paths: M = 1 runs integer dot products (dp4a) on exact block-floating-point
- * activation digits; 2 <= M <= 8 a CUDA-core split-K GEMV (bf16 x bf16 -> fp32 FMA);
- * 9 <= M <= 16 with fewer 128-row tiles than three quarters of the SMs a tcgen05 kernel
- * that splits K across tensor-memory lanes; otherwise a tcgen05 tensor-core GEMM
- * (bf16 x bf16 -> fp32 in tensor memory) on weight tiles dequantized into tensor memory.
- * Shapes a fast path cannot take (K not a multiple of 2048, unaligned scale or zero
- * tables) run a plain CUDA-core kernel.
+ * activation digits; 2 <= M <= 16 warp-level tensor-core MMAs (bf16 x bf16 -> fp32)
+ * on weights dequantized in registers, when K is a multiple of 2048 and the activations
+ * fit in shared memory; otherwise 9 <= M <= 16 with fewer 128-row tiles than three
+ * quarters of the SMs a tcgen05 kernel that splits K across tensor-memory lanes, and
+ * larger M a tcgen05 tensor-core GEMM (bf16 x bf16 -> fp32 in tensor memory) on weight
+ * tiles dequantized into tensor memory.  Shapes a fast path cannot take (K not a
+ * multiple of 2048, unaligned scale or zero tables) run a plain CUDA-core kernel.
  *
  * Arguments:
  *   A        device pointer, bf16 [M, K]; 16-byte aligned.
@@ -162,6 +232,60 @@ W4_API int w4_dequantize(const uint8_t *qweight, const void *scales, const uint8
 W4_API int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group,
               const uint8_t *qweight, const void *scales, const uint8_t *zeros,
               void *Y, cudaStream_t stream);
+
+/*
+ * w4_quantize_act_int8 -- per-token INT8 dynamic quantization of the activations (the
+ * A8 of W4A8).
+ *
+ * Defined by: "Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with
+ * Per-Channel Scale" (Step 3, activations_to_int8: per token, scale = max|A| / 127 with
+ * max|A| clipped below at 1e-8, levels round(A / scale) clipped to [-128, 127]).  Exact
+ * convention, per row m of A, values widened exactly to fp32:
+ *     a_scale[m] = max(max_k |A[m,k]|, 1e-8) / 127          (IEEE fp32 division)
+ *     a_q[m,k]   = clip(round_half_even(A[m,k] / a_scale[m]), -128, 127)
+ * Bit-exact for finite A (|a_q| <= 127 then).
+ *
+ * Arguments:
+ *   A        device pointer, bf16 [M, K]; 16-byte aligned.
+ *   M, K     M >= 0, K >= 0, K % 8 == 0.
+ *   a_q      device pointer, int8 [M, K]; 16-byte aligned.  Written.
+ *   a_scale  device pointer, fp32 [M]; 4-byte aligned.  Written.
+ *   stream   the stream to run on.
+ * M == 0: W4_OK, nothing launched.
+ */
+W4_API int w4_quantize_act_int8(const void *A, int64_t M, int64_t K, int8_t *a_q, float *a_scale,
+                                cudaStream_t stream);
+
+/*
+ * w4_matmul_w4a8 -- Y[M,N] = a_scale[m] * sum_k a_q[m,k] * W_hat[n,k] with W_hat =
+ * (q - zp) * scale_fp16, fp32 accumulation, output rounded to nearest-even bf16: the
+ * W4A8 forward pass over per-token INT8 activations.
+ *
+ * Defined by: "Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with
+ * Per-Channel Scale" (Step 5, forward_quant: the INT8 activations times their per-token
+ * scale, multiplied by the dequantized INT4 weights).  Accuracy contract per element:
+ *     |Y - Y_exact| <= 8e-3 * sum_k |a_q[m,k] a_scale[m] W_hat[n,k]| + ulp_bf16(|Y_exact|) / 2.
+ * The int8 x int4 products are exact in bf16 x bf16 -> fp32, so the contraction runs on
+ * the bf16 tensor pipe (this part's int8 tensor rate is far below its bf16 rate):
+ *   1 <= M <= 16, K a multiple of 2048 (activations fitting in shared memory): the
+ *     decode kernel of w4_matmul, a_q widened to bf16 while staged; no workspace.
+ *   otherwise: a_q is widened to bf16 into `workspace` and the tcgen05 GEMM of w4_matmul
+ *     runs with a_scale applied to each output row before rounding.
+ *
+ * Arguments:
+ *   a_q, a_scale  as written by w4_quantize_act_int8 (a_q 16-byte aligned).
+ *   M, N, K, group, qweight, scales, zeros, Y  as w4_matmul; on the decode path scales
+ *            and zeros must be 16-byte aligned (W4_ERR_MISALIGNED otherwise).
+ *   workspace  device pointer to at least w4_matmul_w4a8_workspace_size(M, K) bytes,
+ *            16-byte aligned, owned by the caller; may be NULL when that size is 0.
+ *            A smaller workspace gives W4_ERR_INVALID_ARG.  Its contents are scratch.
+ *   stream   the stream to run on.
+ * M == 0 or N == 0: W4_OK, nothing launched.  K == 0: Y is filled with zeros.
+ */
+W4_API size_t w4_matmul_w4a8_workspace_size(int64_t M, int64_t K);
+W4_API int w4_matmul_w4a8(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N, int64_t K,
+                          int group, const uint8_t *qweight, const void *scales, const uint8_t *zeros,
+                          void *Y, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* A static, human-readable name for a status code (never NULL). */
 W4_API const char *w4_status_string(int status);

@@ -74,6 +74,8 @@ def _load():
     lib.oracle_quantize_act_int8.restype = ctypes.c_int
     lib.oracle_w4a8_matmul.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, dp, dp]
     lib.oracle_w4a8_matmul.restype = ctypes.c_int
+    lib.oracle_w4a8_matmul_entries.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, i64, dp, dp]
+    lib.oracle_w4a8_matmul_entries.restype = ctypes.c_int
     lib.oracle_gptq_quantize.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
     lib.oracle_gptq_quantize.restype = ctypes.c_int
     lib.oracle_dequantize_16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, vp]
@@ -315,6 +317,25 @@ def w4a8_matmul(a_q: np.ndarray, a_scale: np.ndarray, qweight, scales, zeros):
     if _load().oracle_w4a8_matmul(_ptr(aq), _ptr(sa), M, N, K, _ptr(qweight), _ptr(s), _ptr(z),
                                   _ptr(Y), _ptr(S)):
         raise RuntimeError("oracle_w4a8_matmul failed")
+    return Y, S
+
+
+def w4a8_matmul_entries(a_q, a_scale, qweight, scales, zeros, mi, ni):
+    """The W4A8 fp64 result and S for the listed (m, n) positions only."""
+    aq = np.ascontiguousarray(a_q, dtype=np.int8)
+    sa = np.ascontiguousarray(a_scale, dtype=np.float32)
+    M, K = aq.shape
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint8)
+    s = _as_u16_bits(scales)
+    z = np.ascontiguousarray(zeros, dtype=np.uint8)
+    N = qweight.shape[0]
+    mi = np.ascontiguousarray(mi, dtype=np.int64)
+    ni = np.ascontiguousarray(ni, dtype=np.int64)
+    Y = np.empty(len(mi), np.float64)
+    S = np.empty(len(mi), np.float64)
+    if _load().oracle_w4a8_matmul_entries(_ptr(aq), _ptr(sa), M, N, K, _ptr(qweight), _ptr(s), _ptr(z),
+                                          _ptr(mi), _ptr(ni), len(mi), _ptr(Y), _ptr(S)):
+        raise RuntimeError("oracle_w4a8_matmul_entries failed")
     return Y, S
 
 

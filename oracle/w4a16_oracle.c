@@ -598,6 +598,32 @@ int oracle_w4a8_matmul(const int8_t *a_q, const float *a_scale, int64_t M, int64
     return rc;
 }
 
+/* The W4A8 product for a list of (m, n) output positions, one by one (checks of
+ * full-size outputs on a sample): Y = sum_k (a_q[m,k] * s_a[m]) * w_hat[n,k] in fp64. */
+int oracle_w4a8_matmul_entries(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N, int64_t K,
+                               const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                               const int64_t *mi, const int64_t *ni, int64_t count, double *Y, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % ORACLE_GROUP != 0) return -1;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    if (!w) return -2;
+    for (int64_t t = 0; t < count; ++t) {
+        int64_t m = mi[t], n = ni[t];
+        if (m < 0 || m >= M || n < 0 || n >= N) { free(w); return -1; }
+        dequant_rows(qweight, scales, zeros, n, 1, K, w);
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = ((double)a_q[m * K + k] * (double)a_scale[m]) * w[k];
+            acc += p;
+            sab += fabs(p);
+        }
+        Y[t] = acc;
+        if (S) S[t] = sab;
+    }
+    free(w);
+    return 0;
+}
+
 /* The same quantity for a list of (m, n) output positions, one by one; used to
  * check full-size outputs on a sample. */
 int oracle_matmul_entries(const uint16_t *A, int64_t M, int64_t N, int64_t K,

@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(w4_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_entry_points():
@@ -158,3 +158,84 @@ def test_binding_fails_loudly_without_library(tmp_path):
             _binding.load_library(str(tmp_path / "missing.so"))
         finally:
             _binding._lib = _binding._lib_saved
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, 0, -1, 128, 128), 1),
+    ((FAKE, 0, 4, 130, 128), 1),
+    ((FAKE, 0, 4, 128, 64), 2),
+    ((FAKE, 7, 4, 128, 128), 1),
+    ((0, 0, 4, 128, 128), 1),
+    ((FAKE + 8, 1, 4, 128, 128), 3),
+    ((FAKE, 0, 0, 128, 128), 0),
+    ((FAKE, 1, 4, 0, 128), 0),
+])
+def test_calibrated_quantizers_validation(lib, args, expect):
+    """The percentile and MSE quantizers validate as w4_quantize_pack, plus their
+    parameter ranges: p in (0, 100], candidates in [1, 2^24]."""
+    W, dt, N, K, G = args
+    assert lib.w4_quantize_pack_percentile(W, dt, N, K, G, ctypes.c_float(99.9), FAKE, FAKE, FAKE, None) == expect
+    assert lib.w4_quantize_pack_mse(W, dt, N, K, G, 1000, FAKE, FAKE, FAKE, None) == expect
+
+
+@pytest.mark.parametrize("p", [0.0, -1.0, 100.5, float("nan"), float("inf")])
+def test_percentile_parameter_range(lib, p):
+    assert lib.w4_quantize_pack_percentile(FAKE, 0, 4, 128, 128, ctypes.c_float(p), FAKE, FAKE, FAKE, None) == 1
+
+
+@pytest.mark.parametrize("n", [0, -5, (1 << 24) + 1])
+def test_mse_candidate_range(lib, n):
+    assert lib.w4_quantize_pack_mse(FAKE, 0, 4, 128, 128, n, FAKE, FAKE, FAKE, None) == 1
+
+
+def test_act_int8_validation(lib):
+    """Per-token activation quantizer: sizes, K % 8, nulls, alignment, empty."""
+    assert lib.w4_quantize_act_int8(FAKE, -1, 128, FAKE, FAKE, None) == 1
+    assert lib.w4_quantize_act_int8(FAKE, 4, 12, FAKE, FAKE, None) == 1
+    assert lib.w4_quantize_act_int8(FAKE, 0, 128, FAKE, FAKE, None) == 0
+    assert lib.w4_quantize_act_int8(0, 4, 128, FAKE, FAKE, None) == 1
+    assert lib.w4_quantize_act_int8(FAKE, 4, 128, FAKE, 0, None) == 1
+    assert lib.w4_quantize_act_int8(FAKE + 8, 4, 128, FAKE, FAKE, None) == 3
+    assert lib.w4_quantize_act_int8(FAKE, 4, 128, FAKE + 8, FAKE, None) == 3
+    assert lib.w4_quantize_act_int8(FAKE, 4, 128, FAKE, FAKE + 2, None) == 3
+
+
+def test_w4a8_workspace_size(lib):
+    """Decode shapes (M <= 16, K a multiple of 2048, activations fitting in shared
+    memory) need no workspace; others need M * K * 2 bytes rounded up to 256."""
+    assert lib.w4_matmul_w4a8_workspace_size(1, 4096) == 0
+    assert lib.w4_matmul_w4a8_workspace_size(16, 4096) == 0
+    assert lib.w4_matmul_w4a8_workspace_size(17, 4096) == 17 * 4096 * 2
+    assert lib.w4_matmul_w4a8_workspace_size(3, 1000 // 8 * 8 + 128 * 8) == -(-3 * 2024 * 2 // 256) * 256
+    assert lib.w4_matmul_w4a8_workspace_size(2048, 4096) == 2048 * 4096 * 2
+    assert lib.w4_matmul_w4a8_workspace_size(0, 4096) == 0
+
+
+def test_w4a8_matmul_validation(lib):
+    args = (FAKE, FAKE, 2, 4, 256, 128, FAKE, FAKE, FAKE, FAKE, 0, 0, None)
+    assert lib.w4_matmul_w4a8(*args[:2], -1, *args[3:]) == 1
+    assert lib.w4_matmul_w4a8(*args[:5], 64, *args[6:]) == 2
+    assert lib.w4_matmul_w4a8(*args[:4], 200, *args[5:]) == 1
+    assert lib.w4_matmul_w4a8(*args[:2], 0, *args[3:]) == 0
+    assert lib.w4_matmul_w4a8(0, *args[1:]) == 1
+    assert lib.w4_matmul_w4a8(FAKE + 8, *args[1:]) == 3
+    assert lib.w4_matmul_w4a8(FAKE, FAKE + 2, *args[2:]) == 3
+    assert lib.w4_matmul_w4a8(*args[:9], FAKE + 1, *args[10:]) == 3
+
+
+def test_gptq_validation(lib):
+    args = [FAKE, 0, 4, 256, 128, FAKE, FAKE, FAKE, FAKE, None]   # never called as is: it would launch
+    bad = list(args); bad[2] = -1
+    assert lib.w4_gptq_quantize(*bad) == 1
+    bad = list(args); bad[4] = 64
+    assert lib.w4_gptq_quantize(*bad) == 2
+    bad = list(args); bad[3] = 200
+    assert lib.w4_gptq_quantize(*bad) == 1
+    bad = list(args); bad[3] = 16384
+    assert lib.w4_gptq_quantize(*bad) == 2
+    bad = list(args); bad[5] = 0
+    assert lib.w4_gptq_quantize(*bad) == 1
+    bad = list(args); bad[5] = FAKE + 4
+    assert lib.w4_gptq_quantize(*bad) == 3
+    bad = list(args); bad[2] = 0
+    assert lib.w4_gptq_quantize(*bad) == 0

@@ -671,3 +671,14 @@ def test_gptq_factor_inverts_the_hessian(oracle_mod):
     H = X.T @ X / 1000
     H += 1e-4 * np.mean(np.diag(H)) * np.eye(256)
     assert np.allclose(U.T @ U @ H, np.eye(256), atol=1e-4)
+
+
+def test_w4a8_entries_equal_the_full_product(oracle_mod):
+    import synth
+    W, A = synth.make_random(40, 384, 5, seed=98)
+    q, s, z = oracle_mod.quantize_pack(W)
+    aq, sa = oracle_mod.quantize_act_int8(A)
+    Y, S = oracle_mod.w4a8_matmul(aq, sa, q, s, z)
+    mi, ni = np.repeat(np.arange(5), 40), np.tile(np.arange(40), 5)
+    Ye, Se = oracle_mod.w4a8_matmul_entries(aq, sa, q, s, z, mi, ni)
+    assert np.array_equal(Ye, Y[mi, ni]) and np.array_equal(Se, S[mi, ni])

@@ -189,6 +189,16 @@ __device__ __forceinline__ void bulk_wait_group0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// ---- programmatic dependent launch --------------------------------------------------
+// Kernels launched with programmatic stream serialization call this before touching
+// global memory: it waits until the preceding kernel in the stream has completed and
+// its writes are visible, then lets the next kernel begin launching (it will wait the
+// same way).  Without that launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- misc ---------------------------------------------------------------------
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 

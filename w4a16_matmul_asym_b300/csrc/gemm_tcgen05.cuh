@@ -300,6 +300,7 @@ struct Params {
     const __half *scales;
     const uint8_t *zeros;
     __nv_bfloat16 *Y;
+    const float *row_scale;  // optional per-activation-row factor applied before rounding (W4A8)
     int M, N, K;
     int mt;          // activation rows per tile (MMA N): multiple of 16, <= 256
     uint32_t idesc;  // instruction descriptor for (M = 128, N = mt)
@@ -473,6 +474,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int j = 0; j < 4; ++j)
                     if (c0 + 8 * j < cols) tmem_ld_8cols(tbase + c0 + 8 * j, v + 8 * j);
                 tmem_wait_ld();
+                if (p.row_scale != nullptr) {
+                    // Column j of this chunk is activation row m0 + c0 + j: scale it in fp32.
+                    const int mr = m0 + c0 + lane;
+                    const float rs = p.row_scale[mr < p.M ? mr : p.M - 1];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), __shfl_sync(0xffffffffu, rs, j)));
+                }
                 if (c0 + 32 >= cols) {
                     // This warp's part of the accumulator is in registers: hand it back.
                     tc_fence_before();
@@ -645,7 +654,8 @@ inline bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ba
 
 inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K,
                                const uint8_t *qweight, const __half *scales, const uint8_t *zeros,
-                               __nv_bfloat16 *Y, cudaStream_t stream, int sms, WaitParams wp) {
+                               __nv_bfloat16 *Y, cudaStream_t stream, int sms, WaitParams wp,
+                               const float *row_scale = nullptr) {
     using namespace gemm;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return W4_ERR_UNSUPPORTED;
     const int mt = static_cast<int>(M >= MT_MAX ? MT_MAX : ((M + 15) / 16) * 16);
@@ -682,6 +692,7 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     prm.scales = scales;
     prm.zeros = zeros;
     prm.Y = Y;
+    prm.row_scale = row_scale;
     prm.M = static_cast<int>(M);
     prm.N = static_cast<int>(N);
     prm.K = static_cast<int>(K);

@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait_then_release();   // no global memory is touched before this point
 
     if (warp == PROD_WARP) {
         // ---------------- producer ----------------

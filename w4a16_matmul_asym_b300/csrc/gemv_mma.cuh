@@ -18,20 +18,34 @@
 // (16 weight rows x 16 k) serves up to 8 activation rows (16 with two MMAs).
 //
 // Data movement.  A tile is 16 rows of W; CTA c owns a contiguous range of tiles (one
-// CTA per SM).  A stage is one tile's 2048-wide k-slice (16 groups), brought in by three
-// tensor copies that complete on the stage's mbarrier: the packed levels through a 3-D
-// tensor map that views qweight as (64 bytes of a group, row, group), so the 16 KB land
-// group-major ([group][row][64 B]: each consumer warp's group is one contiguous 1 KB
-// block, and the 8 lanes of a quarter warp read 128 contiguous bytes); the 16 x 16
-// scales and zero points through 2-D maps.  Rows past N are zero-filled by the copy.
-// Up to MAX_STAGES stages are in flight.  The activations are copied once per CTA into
-// shared memory, permuted so that every B fragment is one conflict-free 16-byte load.
+// CTA per SM).  A stage is one tile's k-slice of 16 * GPW groups (GPW = 2 when K is a
+// multiple of 4096, else 1), brought in by three tensor copies that complete on the
+// stage's mbarrier: the packed levels through a 3-D tensor map that views qweight as
+// (128 bytes = 2 groups, row, group pair), box (128, 16, 8 GPW), with 128-byte swizzle,
+// so they land as [pair][row][128 B] with the 16-byte chunk c of row r stored at
+// c ^ (r & 7); the scales and zero points through 2-D maps.  Rows past N are
+// zero-filled by the copy.  Up to MAX_STAGES stages are in flight.  The activations
+// are copied once per CTA into shared memory, permuted so that every B fragment is one
+// conflict-free 16-byte load (int8 activations, for W4A8, are widened to bf16 there:
+// exact, since |a_q| <= 128).
 //
-// Work split.  Consumer warp w takes quantization group w of every stage (the 16
-// groups of a 2048-wide slice), i.e. split-K across the 16 warps; its partial sums of
-// a tile stay in registers across the tile's stages and go to a double-buffered
-// reduction area at the tile's end; an epilogue warp adds the 16 partials in a fixed
-// order (deterministic), rounds to bf16 and stores Y.
+// Bank conflicts.  The 8 lanes of a quarter warp read MMA rows g and g + 1 (4 chunks
+// each).  MMA row g reads physical row pi(g) = (g >> 1) + 4 (g & 1) of the tile (and
+// g + 8 reads pi(g) + 8), so the two rows of a quarter warp differ in bit 2 and their
+// swizzled chunks fall in opposite halves of the 128-byte bank window.  The output of
+// MMA row g is written back as row pi(g).
+//
+// Work split.  Consumer warp w takes quantization groups w + 16 j (j < GPW) of every
+// stage, i.e. split-K across the 16 warps, with GPW independent dependency chains per
+// warp to hide the latency of shared-memory loads and MMAs; its partial sums of a tile
+// stay in registers across the tile's stages and go to a double-buffered reduction
+// area at the tile's end; an epilogue warp adds the 16 partials in a fixed order
+// (deterministic), applies the optional per-row factor (the W4A8 activation scale),
+// rounds to bf16 and stores Y.
+//
+// Launch: with programmatic dependent launch, so the next kernel's launch overlaps this
+// one's tail; every thread waits (griddepcontrol.wait) for the preceding kernel in the
+// stream before touching global memory.
 //
 // Fragment mapping (m16n8k16, A row-major = W rows, B column-major = activation rows):
 // lane (g, t) = (lane / 4, lane % 4) holds W rows g and g + 8 and, of each group, the
@@ -54,34 +68,44 @@
 namespace w4 {
 namespace gmma {
 
-constexpr int CW = 16;                        // consumer warps = groups per stage
+constexpr int CW = 16;                        // consumer warps
 constexpr int PRODUCER = CW;                  // warp index of the producer
 constexpr int EPILOGUE = CW + 1;              // warp index of the epilogue
 constexpr int NUM_THREADS = (CW + 2) * 32;
 constexpr int ROWS = 16;                      // W rows per tile (the MMA's M)
-constexpr int KC = CW * 128;                  // k per stage
-constexpr int GROUP_BYTES = 64;               // packed bytes of one group of one row
-constexpr int SLOT_W = CW * ROWS * GROUP_BYTES;  // [group][row][64 B]
-constexpr int SLOT_S = ROWS * CW * 2;         // fp16 scales [row][group]
-constexpr int SLOT_Z = ROWS * CW;             // uint8 zero points [row][group]
-constexpr int SLOT_BYTES = SLOT_W + SLOT_S + SLOT_Z;
+constexpr int PAIR_BYTES = 128;               // packed bytes of two groups of one row
 constexpr int MAX_STAGES = 12;
 constexpr int RED_STRIDE = 20;                // floats per (warp, column): conflict-free writes
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr uint32_t kBf16x2_128 = 0x43004300u;  // bf16 pair (128, 128)
 
+// Stage geometry for GPW groups per warp per stage.
+__host__ __device__ constexpr int groups_per_stage(int gpw) { return CW * gpw; }
+__host__ __device__ constexpr int k_per_stage(int gpw) { return 128 * CW * gpw; }
+__host__ __device__ constexpr int slot_w(int gpw) { return ROWS * 64 * CW * gpw; }   // [pair][row][128 B]
+__host__ __device__ constexpr int slot_s(int gpw) { return ROWS * CW * gpw * 2; }    // fp16 [row][group]
+__host__ __device__ constexpr int slot_z(int gpw) { return ROWS * CW * gpw; }        // uint8 [row][group]
+__host__ __device__ constexpr int slot_sz(int gpw) { return slot_s(gpw) + slot_z(gpw); }
+__host__ __device__ constexpr int slot_bytes(int gpw) { return slot_w(gpw) + slot_sz(gpw); }
+
 __host__ __device__ constexpr int red_bytes(int nb) { return 2 * CW * 8 * nb * RED_STRIDE * 4; }
-__host__ __device__ constexpr int a_bytes(int M, int K) { return (M * K * 2 + 127) / 128 * 128; }
+__host__ __device__ constexpr int a_bytes(int M, int K) { return (M * K * 2 + 1023) / 1024 * 1024; }
 __host__ __device__ constexpr int bar_bytes() { return (2 * MAX_STAGES + 5) * 8 + 16; }
-__host__ __device__ constexpr int smem_bytes(int M, int K, int nb, int stages) {
-    return a_bytes(M, K) + stages * SLOT_BYTES + red_bytes(nb) + bar_bytes();
+// Layout (offsets from a 1024-byte aligned base): activations (bf16, permuted), the W
+// parts of every stage (1024-byte aligned for the swizzle), their scale/zero parts, the
+// reduction area, the barriers; plus 1024 bytes of slack for aligning the base.
+__host__ __device__ constexpr int smem_bytes(int M, int K, int nb, int gpw, int stages) {
+    return 1024 + a_bytes(M, K) + stages * slot_bytes(gpw) + red_bytes(nb) + bar_bytes();
 }
+// MMA row g (0..7) reads physical tile row pi(g); rows g + 8 read pi(g) + 8.
+__host__ __device__ constexpr int row_of(int g) { return (g >> 1) + 4 * (g & 1); }
 
 struct Params {
-    const __nv_bfloat16 *A;   // [M, K]
+    const void *A;            // [M, K]: bf16 activations, or int8 ones (W4A8)
     const uint8_t *qweight;   // [N, K/2]
     const __half *scales;     // [N, K/128]
     const uint8_t *zeros;     // [N, K/128]
+    const float *row_scale;   // [M] factor applied to each output row before rounding, or null
     __nv_bfloat16 *Y;         // [M, N]
     int M, N, K;
     int tiles;                // ceil(N / 16)
@@ -125,6 +149,20 @@ __device__ __forceinline__ uint4 pair_permute(const uint4 &nat) {
     r.y = prmt(nat.x, nat.z, 0x7632u);
     r.z = prmt(nat.y, nat.w, 0x5410u);
     r.w = prmt(nat.y, nat.w, 0x7632u);
+    return r;
+}
+// 8 consecutive int8 (natural order) -> the same (k, k+4) bf16 pairs, exactly.
+__device__ __forceinline__ uint32_t bf16x2_of_i8(uint32_t lo_byte, uint32_t hi_byte) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(static_cast<float>(static_cast<int8_t>(lo_byte & 0xFFu)),
+                                                   static_cast<float>(static_cast<int8_t>(hi_byte & 0xFFu)));
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+__device__ __forceinline__ uint4 pair_permute_i8(uint2 nat) {
+    uint4 r;
+    r.x = bf16x2_of_i8(nat.x, nat.y);              // a0, a4
+    r.y = bf16x2_of_i8(nat.x >> 8, nat.y >> 8);    // a1, a5
+    r.z = bf16x2_of_i8(nat.x >> 16, nat.y >> 16);  // a2, a6
+    r.w = bf16x2_of_i8(nat.x >> 24, nat.y >> 24);  // a3, a7
     return r;
 }
 // (x & 0x000F000F) | bf16x2(128, 128): levels at bits [0,4) and [16,20) -> bf16(128 + q).
@@ -177,13 +215,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// One thread issues every stage: three tensor copies (x coordinates 0 and 16 ks, both
-// multiples of 16 bytes).
+// One thread issues every stage: three tensor copies (x coordinates 0 and 16 GPW ks,
+// both multiples of 16 bytes).
+template <int GPW>
 __device__ __forceinline__ void produce(const Params &p, const CUtensorMap *tmW, const CUtensorMap *tmS,
-                                        const CUtensorMap *tmZ, uint8_t *ring, uint64_t *full, uint64_t *empty,
-                                        volatile int *abort_flag, int t_begin, int nstages) {
+                                        const CUtensorMap *tmZ, uint8_t *ring_w, uint8_t *ring_sz, uint64_t *full,
+                                        uint64_t *empty, volatile int *abort_flag, int t_begin, int nstages) {
     if (lane_id() != 0) return;
-    const int KS = p.K / KC, S = p.stages;
+    constexpr int GPS = groups_per_stage(GPW);
+    const int KS = p.K / k_per_stage(GPW), S = p.stages;
     const unsigned long long tmo = p.wait.timeout_ns;
     const uint64_t pol = policy_evict_first();
     uint32_t slot = 0, phase = 0;
@@ -196,11 +236,11 @@ __device__ __forceinline__ void produce(const Params &p, const CUtensorMap *tmW,
         }
         const int tile = t_begin + i / KS, ks = i % KS;
         const int n0 = tile * ROWS;
-        uint8_t *st = ring + static_cast<size_t>(slot) * SLOT_BYTES;
-        mbar_arrive_expect_tx(&full[slot], SLOT_BYTES);
-        tma_load_3d(st, tmW, &full[slot], 0, n0, ks * CW, pol);
-        tma_load_2d(st + SLOT_W, tmS, &full[slot], ks * CW, n0, pol);
-        tma_load_2d(st + SLOT_W + SLOT_S, tmZ, &full[slot], ks * CW, n0, pol);
+        uint8_t *sz = ring_sz + static_cast<size_t>(slot) * slot_sz(GPW);
+        mbar_arrive_expect_tx(&full[slot], slot_bytes(GPW));
+        tma_load_3d(ring_w + static_cast<size_t>(slot) * slot_w(GPW), tmW, &full[slot], 0, n0, ks * (GPS / 2), pol);
+        tma_load_2d(sz, tmS, &full[slot], ks * GPS, n0, pol);
+        tma_load_2d(sz + slot_s(GPW), tmZ, &full[slot], ks * GPS, n0, pol);
         ++issued;
         if (++slot == static_cast<uint32_t>(S)) {
             slot = 0;
@@ -228,6 +268,12 @@ __device__ __forceinline__ void epilogue(const Params &p, const float *red, uint
     const int lane = lane_id();
     const int r = lane & 15;
     const unsigned long long tmo = p.wait.timeout_ns;
+    float rs[COLS / 2];
+#pragma unroll
+    for (int i = 0; i < COLS / 2; ++i) {
+        const int m = (lane >> 4) + 2 * i;
+        rs[i] = (p.row_scale != nullptr && m < p.M) ? p.row_scale[m] : 1.0f;
+    }
     for (int j = 0; j < ntiles; ++j) {
         const int b = j & 1;
         if (!warp_wait(&red_full[b], static_cast<uint32_t>((j >> 1) & 1), abort_flag, tmo, true)) return;
@@ -248,25 +294,31 @@ __device__ __forceinline__ void epilogue(const Params &p, const float *red, uint
 #pragma unroll
             for (int i = 0; i < COLS / 2; ++i) {
                 const int m = (lane >> 4) + 2 * i;
-                if (m < p.M) p.Y[static_cast<int64_t>(m) * p.N + n] = __float2bfloat16_rn(acc[i]);
+                if (m < p.M) p.Y[static_cast<int64_t>(m) * p.N + n] = __float2bfloat16_rn(__fmul_rn(acc[i], rs[i]));
             }
         }
     }
 }
 
 // ---- the kernel ----------------------------------------------------------------------------
-// NB = number of 8-column activation blocks (1: M <= 8, 2: M <= 16).
-template <int NB>
+// NB = number of 8-column activation blocks (1: M <= 8, 2: M <= 16); GPW = groups per
+// warp per stage; I8 = int8 activations (widened to bf16 while staged).
+template <int NB, int GPW, bool I8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                     const __grid_constant__ CUtensorMap tmZ, const Params p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // The 128-byte swizzle of the W copies assumes 1024-byte aligned shared offsets.
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     constexpr int COLS = 8 * NB;
+    constexpr int GPS = groups_per_stage(GPW);
+    constexpr int SW = slot_w(GPW), SSZ = slot_sz(GPW), SS = slot_s(GPW);
     const int M = p.M, K = p.K;
-    const int KS = K / KC;
+    const int KS = K / k_per_stage(GPW);
     const int S = p.stages;
-    uint8_t *ring = smem + a_bytes(M, K);
-    float *red = reinterpret_cast<float *>(ring + static_cast<size_t>(S) * SLOT_BYTES);
+    uint8_t *ring_w = smem + a_bytes(M, K);
+    uint8_t *ring_sz = ring_w + static_cast<size_t>(S) * SW;
+    float *red = reinterpret_cast<float *>(ring_sz + static_cast<size_t>(S) * SSZ);
     uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(red) + red_bytes(NB));
     uint64_t *empty = full + MAX_STAGES;
     uint64_t *red_full = empty + MAX_STAGES;
@@ -298,9 +350,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tensormap(&tmZ);
     }
     __syncthreads();
+    pdl_wait_then_release();   // no global memory is touched before this point
 
     if (warp == PRODUCER) {
-        produce(p, &tmW, &tmS, &tmZ, ring, full, empty, abort_flag, t_begin, nstages);
+        produce<GPW>(p, &tmW, &tmS, &tmZ, ring_w, ring_sz, full, empty, abort_flag, t_begin, nstages);
         return;
     }
     if (warp == EPILOGUE) {
@@ -309,8 +362,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     // ---- consumers: stage the activations, permuted: the 16-byte chunk (g, v, m, t)
-    // (index ((4 g + v) M + m) 4 + t) holds A[m, 128 g + 32 t + 8 v + (0 4 1 5 2 6 3 7)].
-    // Threads walk the chunks in shared-memory order, so the stores are conflict-free.
+    // (index ((4 g + v) M + m) 4 + t) holds A[m, 128 g + 32 t + 8 v + (0 4 1 5 2 6 3 7)]
+    // as bf16.  Threads walk the chunks in shared-memory order, so the stores are
+    // conflict-free.
     const uint32_t a_base = smem_addr(smem);
     {
         const int total = M * (K >> 3);
@@ -325,14 +379,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int t = c & 3, rest = c >> 2;
                     const int m = rest % M, gv = rest / M;
                     const int g = gv >> 2, v = gv & 3;
-                    nat[u] = __ldg(reinterpret_cast<const uint4 *>(p.A + static_cast<int64_t>(m) * K + g * 128 +
-                                                                   t * 32 + v * 8));
+                    const int64_t e = static_cast<int64_t>(m) * K + g * 128 + t * 32 + v * 8;
+                    if constexpr (I8) {
+                        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(p.A) + e));
+                        nat[u] = make_uint4(q.x, q.y, 0, 0);
+                    } else {
+                        nat[u] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.A) + e));
+                    }
                 }
             }
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
                 const int c = c0 + u * CW * 32;
-                if (c < total) sts128(a_base + (static_cast<uint32_t>(c) << 4), pair_permute(nat[u]));
+                if (c < total) {
+                    uint4 v;
+                    if constexpr (I8) v = pair_permute_i8(make_uint2(nat[u].x, nat[u].y));
+                    else v = pair_permute(nat[u]);
+                    sts128(a_base + (static_cast<uint32_t>(c) << 4), v);
+                }
             }
         }
     }
@@ -342,13 +406,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (p.wait.stall) ok = warp_wait(never, 0, abort_flag, tmo, false);  // test hook
 
     const int g8 = lane >> 2, t4 = lane & 3;
-    const uint32_t ring_base = smem_addr(ring);
-    const uint32_t w_off0 = warp * (ROWS * GROUP_BYTES) + g8 * GROUP_BYTES + t4 * 16;
-    const uint32_t w_off1 = w_off0 + 8 * GROUP_BYTES;
-    const uint32_t s_off0 = SLOT_W + g8 * (CW * 2) + warp * 2;
-    const uint32_t s_off1 = s_off0 + 8 * (CW * 2);
-    const uint32_t z_off0 = SLOT_W + SLOT_S + g8 * CW + warp;
-    const uint32_t z_off1 = z_off0 + 8 * CW;
+    const int r0 = row_of(g8), r1 = r0 + 8;        // physical rows of MMA rows g8, g8 + 8
+    const uint32_t ringw_base = smem_addr(ring_w), ringsz_base = smem_addr(ring_sz);
+    // Group w + 16 j of a stage sits in pair (w >> 1) + 8 j, half w & 1: its 16-byte chunk
+    // c = 4 (w & 1) + t4, swizzled by r & 7 (the same for r0 and r1).
+    const uint32_t chunk = static_cast<uint32_t>(((warp & 1) * 4 + t4) ^ (r0 & 7)) << 4;
+    const uint32_t w_off0 = (warp >> 1) * (ROWS * PAIR_BYTES) + r0 * PAIR_BYTES + chunk;
+    constexpr uint32_t W_J = 8 * ROWS * PAIR_BYTES;   // offset of group w + 16 from group w
     float y[NB][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
@@ -362,11 +426,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
         }
-        const uint32_t st = ring_base + slot * SLOT_BYTES;
-        const uint4 w0 = lds128(st + w_off0);
-        const uint4 w1 = lds128(st + w_off1);
-        const uint32_t s0 = lds_u16(st + s_off0), s1 = lds_u16(st + s_off1);
-        const uint32_t z0 = lds_u8(st + z_off0), z1 = lds_u8(st + z_off1);
+        const uint32_t stw = ringw_base + slot * SW, stsz = ringsz_base + slot * SSZ;
+        uint32_t wa[GPW][4], wb[GPW][4], zz0[GPW], zz1[GPW];
+        float sf0[GPW], sf1[GPW];
+#pragma unroll
+        for (int h = 0; h < GPW; ++h) {
+            const int gs = warp + CW * h;
+            const uint4 w0 = lds128(stw + w_off0 + h * W_J);
+            const uint4 w1 = lds128(stw + w_off0 + h * W_J + 8 * PAIR_BYTES);
+            wa[h][0] = w0.x; wa[h][1] = w0.y; wa[h][2] = w0.z; wa[h][3] = w0.w;
+            wb[h][0] = w1.x; wb[h][1] = w1.y; wb[h][2] = w1.z; wb[h][3] = w1.w;
+            sf0[h] = half_bits_to_f32(lds_u16(stsz + r0 * (GPS * 2) + gs * 2));
+            sf1[h] = half_bits_to_f32(lds_u16(stsz + r1 * (GPS * 2) + gs * 2));
+            zz0[h] = kBf16x2_128 + lds_u8(stsz + SS + r0 * GPS + gs) * 0x00010001u;  // bf16 pair (128 + zp)
+            zz1[h] = kBf16x2_128 + lds_u8(stsz + SS + r1 * GPS + gs) * 0x00010001u;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         if (++slot == static_cast<uint32_t>(S)) {
@@ -374,50 +448,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             phase ^= 1u;
         }
 
-        // B fragments of this group for my activation rows g8 (+ 8).
-        const int g = ks * CW + warp;
-        uint4 bf[NB][4];
+        float d[GPW][NB][2][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const int m = g8 + 8 * nb;
+        for (int h = 0; h < GPW; ++h)
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                bf[nb][v] = m < M ? lds128(a_base + ((((g * 4 + v) * M + m) * 4 + t4) << 4)) : make_uint4(0, 0, 0, 0);
-        }
-
-        const uint32_t zz0 = kBf16x2_128 + z0 * 0x00010001u;   // bf16 pair (128 + zp)
-        const uint32_t zz1 = kBf16x2_128 + z1 * 0x00010001u;
-        float d[NB][2][4];
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
+                for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d[nb][h][e] = 0.0f;
-        const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
-        const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
+                    for (int e = 0; e < 4; ++e) d[h][nb][q][e] = 0.0f;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-            uint32_t pa[4], pb[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                pa[k] = bsub2(level_pair(wa[v] >> (4 * k)), zz0);
-                pb[k] = bsub2(level_pair(wb[v] >> (4 * k)), zz1);
+            for (int h = 0; h < GPW; ++h) {
+                const int g = ks * GPS + warp + CW * h;   // group within the row
+                uint32_t pa[4], pb[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    pa[k] = bsub2(level_pair(wa[h][v] >> (4 * k)), zz0[h]);
+                    pb[k] = bsub2(level_pair(wb[h][v] >> (4 * k)), zz1[h]);
+                }
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    const int m = g8 + 8 * nb;
+                    const uint4 bf = m < M ? lds128(a_base + ((((g * 4 + v) * M + m) * 4 + t4) << 4))
+                                           : make_uint4(0, 0, 0, 0);
+                    mma_bf16(d[h][nb][0], pa[0], pb[0], pa[1], pb[1], bf.x, bf.y);
+                    mma_bf16(d[h][nb][1], pa[2], pb[2], pa[3], pb[3], bf.z, bf.w);
+                }
             }
+        }
+#pragma unroll
+        for (int h = 0; h < GPW; ++h)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                mma_bf16(d[nb][0], pa[0], pb[0], pa[1], pb[1], bf[nb][v].x, bf[nb][v].y);
-                mma_bf16(d[nb][1], pa[2], pb[2], pa[3], pb[3], bf[nb][v].z, bf[nb][v].w);
+                y[nb][0] = fmaf(sf0[h], __fadd_rn(d[h][nb][0][0], d[h][nb][1][0]), y[nb][0]);
+                y[nb][1] = fmaf(sf0[h], __fadd_rn(d[h][nb][0][1], d[h][nb][1][1]), y[nb][1]);
+                y[nb][2] = fmaf(sf1[h], __fadd_rn(d[h][nb][0][2], d[h][nb][1][2]), y[nb][2]);
+                y[nb][3] = fmaf(sf1[h], __fadd_rn(d[h][nb][0][3], d[h][nb][1][3]), y[nb][3]);
             }
-        }
-        const float sf0 = half_bits_to_f32(s0), sf1 = half_bits_to_f32(s1);
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            y[nb][0] = fmaf(sf0, __fadd_rn(d[nb][0][0], d[nb][1][0]), y[nb][0]);
-            y[nb][1] = fmaf(sf0, __fadd_rn(d[nb][0][1], d[nb][1][1]), y[nb][1]);
-            y[nb][2] = fmaf(sf1, __fadd_rn(d[nb][0][2], d[nb][1][2]), y[nb][2]);
-            y[nb][3] = fmaf(sf1, __fadd_rn(d[nb][0][3], d[nb][1][3]), y[nb][3]);
-        }
 
         if (ks == KS - 1) {  // tile done: partial sums to the reduction area
             const int b = j & 1;
@@ -429,10 +498,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
                 const int c = 8 * nb + 2 * t4;
-                rb[c * RED_STRIDE + g8] = y[nb][0];
-                rb[(c + 1) * RED_STRIDE + g8] = y[nb][1];
-                rb[c * RED_STRIDE + g8 + 8] = y[nb][2];
-                rb[(c + 1) * RED_STRIDE + g8 + 8] = y[nb][3];
+                rb[c * RED_STRIDE + r0] = y[nb][0];
+                rb[(c + 1) * RED_STRIDE + r0] = y[nb][1];
+                rb[c * RED_STRIDE + r1] = y[nb][2];
+                rb[(c + 1) * RED_STRIDE + r1] = y[nb][3];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) y[nb][e] = 0.0f;
             }
@@ -442,26 +511,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// Tensor maps of one launch: qweight as (64 B, row, group) with box (64, 16, 16); scales
-// and zero points as [row][group] with box (16 groups, 16 rows).  Strides are multiples
-// of 16 bytes when K is a multiple of 2048 and the bases are 16-byte aligned.
+// Tensor maps of one launch: qweight as (128 B, row, group pair) with box (128, 16, 8 GPW)
+// and 128-byte swizzle; scales and zero points as [row][group] with box (16 GPW groups,
+// 16 rows).  Strides are multiples of 16 bytes when K is a multiple of 2048 and the bases
+// are 16-byte aligned.
 inline bool make_maps(CUtensorMap *tmW, CUtensorMap *tmS, CUtensorMap *tmZ, const uint8_t *qweight,
-                      const __half *scales, const uint8_t *zeros, int64_t N, int64_t K) {
+                      const __half *scales, const uint8_t *zeros, int64_t N, int64_t K, int gpw) {
     auto fn = gemm::encode_fn();
     if (!fn) return false;
     const uint64_t ng = static_cast<uint64_t>(K / 128);
-    const cuuint64_t wd[3] = {GROUP_BYTES, static_cast<cuuint64_t>(N), ng};
-    const cuuint64_t ws[2] = {static_cast<cuuint64_t>(K / 2), GROUP_BYTES};
-    const cuuint32_t wb[3] = {GROUP_BYTES, ROWS, CW};
+    const cuuint64_t wd[3] = {PAIR_BYTES, static_cast<cuuint64_t>(N), ng / 2};
+    const cuuint64_t ws[2] = {static_cast<cuuint64_t>(K / 2), PAIR_BYTES};
+    const cuuint32_t wb[3] = {PAIR_BYTES, ROWS, static_cast<cuuint32_t>(8 * gpw)};
     const cuuint32_t es[3] = {1, 1, 1};
     if (fn(tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(qweight), wd, ws, wb, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
-    return gemm::make_map_2d(tmS, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, ng, N, ng * 2, CW, ROWS,
+    const uint32_t gps = static_cast<uint32_t>(groups_per_stage(gpw));
+    return gemm::make_map_2d(tmS, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, ng, N, ng * 2, gps, ROWS,
                              CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           gemm::make_map_2d(tmZ, CU_TENSOR_MAP_DATA_TYPE_UINT8, zeros, ng, N, ng, CW, ROWS,
+           gemm::make_map_2d(tmZ, CU_TENSOR_MAP_DATA_TYPE_UINT8, zeros, ng, N, ng, gps, ROWS,
                              CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Groups per warp per stage and ring depth for a shape, or 0 stages if it does not fit.
+inline void plan(int M, int K, int *gpw, int *stages) {
+    const int nb = M <= 8 ? 1 : 2;
+    *gpw = (nb == 1 && K % k_per_stage(2) == 0) ? 2 : 1;
+    *stages = 0;
+    for (int s = MAX_STAGES; s >= 2; --s)
+        if (smem_bytes(M, K, nb, *gpw, s) <= SMEM_LIMIT) {
+            *stages = s;
+            return;
+        }
 }
 
 }  // namespace gmma

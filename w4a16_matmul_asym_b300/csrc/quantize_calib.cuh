@@ -1,0 +1,211 @@
+// quantize_calib.cuh -- clip-range calibrated symmetric INT4 quantization + packing.
+//
+// Method ("Building a From-Scratch Group-Wise INT4 Quantization Layer for LLaMA
+// Weights", Step 4, ScaleCalibrator), per group of 128 elements along K, values
+// widened exactly to fp32:
+//   percentile: r = the p-th percentile of |w|, linear interpolation between the
+//     ascending order statistics a_0 <= ... <= a_127 in fp32: h = fl(fl(p / 100) * 127),
+//     lo = floor(h), f = h - lo, r = a_lo + f * (a_(lo+1) - a_lo); step s = r / 7
+//     (1 when r == 0).
+//   mse: the step is searched over n candidates c_i = linspace(min|w|, max|w|, n)
+//     (c_i = fl(min + fl(i * fl((max - min) / (n - 1)))), the last one max itself, the
+//     only one min when n == 1); candidates below 1e-10 are skipped; each scores
+//     fl(e / 128) with e the fp32 sum, in index order, of fl(d * d), d = fl(fl(t * c) - w),
+//     t = clamp(rint(w / c), -7, 7); the first candidate with the smallest score wins
+//     (1e-8 if none is scored).
+//   Both: level = clamp(rint(w / s), -7, 7) + 8, zero point 8, scale = rne fp16(s), the
+//   layout of w4_quantize_pack, so w4_matmul and w4_dequantize consume the result.
+// Every step is an IEEE fp32 operation with round-to-nearest-even (the quotients by
+// __fdiv_rn, the roundings to integers by rint), in the order above, so the result is
+// bit-exact with a sequential fp32 evaluation.
+//
+// Mapping: one warp per group, lane l holding elements 4l .. 4l+3; a grid-stride loop
+// over the flat group index G (W elements [128 G, 128 G + 128), qweight bytes
+// [64 G, 64 G + 64), scales[G], zeros[G]).
+//   percentile: the warp sorts the 128 magnitudes with a bitonic network (registers and
+//     xor-shuffles) and reads the two order statistics it needs.
+//   mse: the group goes to shared memory; lane l scores candidates l, l + 32, ... over
+//     all 128 elements (broadcast reads), keeping its first minimum; a warp reduction
+//     takes the smallest score, ties to the lower candidate index.  This is ALU work:
+//     n * 128 quotients per group.
+#pragma once
+
+#include <climits>
+
+#include "common.cuh"
+
+namespace w4 {
+namespace calib {
+
+constexpr int WARPS = 8;
+constexpr int NUM_THREADS = WARPS * 32;
+
+struct Params {
+    const void *W;        // fp16 or fp32 [N, K]
+    int64_t groups;       // N * K / 128
+    uint8_t *qweight;     // [N, K/2]
+    __half *scales;       // [N, K/128]
+    uint8_t *zeros;       // [N, K/128]
+    float p;              // percentile, 0 < p <= 100
+    int n;                // MSE candidates, >= 1
+};
+
+template <bool kF32>
+__device__ __forceinline__ void load_group4(const void *W, int64_t g, int lane, float (&w)[4]) {
+    if constexpr (kF32) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(W) + g * 32 + lane);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(W) + g * 32 + lane);
+        w[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(v.x & 0xFFFFu)));
+        w[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(v.x >> 16)));
+        w[2] = __half2float(__ushort_as_half(static_cast<unsigned short>(v.y & 0xFFFFu)));
+        w[3] = __half2float(__ushort_as_half(static_cast<unsigned short>(v.y >> 16)));
+    }
+}
+
+// clamp(rint(w / s), -7, 7) + 8
+__device__ __forceinline__ uint32_t level7(float w, float s) {
+    const float t = fminf(fmaxf(rintf(__fdiv_rn(w, s)), -7.0f), 7.0f);
+    return static_cast<uint32_t>(static_cast<int>(t) + 8);
+}
+
+// Levels of the lane's 4 elements -> 2 packed bytes; lane 0 also writes scale and zp.
+__device__ __forceinline__ void store_group(const Params &p, int64_t g, int lane, const float (&w)[4], float s) {
+    const uint32_t v = level7(w[0], s) | (level7(w[1], s) << 4) | (level7(w[2], s) << 8) | (level7(w[3], s) << 12);
+    reinterpret_cast<uint16_t *>(p.qweight + g * 64)[lane] = static_cast<uint16_t>(v);
+    if (lane == 0) {
+        p.scales[g] = __float2half_rn(s);
+        p.zeros[g] = 8;
+    }
+}
+
+// Ascending bitonic sort of the warp's 128 values (element e = 4 lane + i in a[i]).
+__device__ __forceinline__ void bitonic128(float (&a)[4], int lane) {
+#pragma unroll
+    for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 4) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = lane * 4 + i;
+                    const float o = __shfl_xor_sync(0xffffffffu, a[i], j >> 2);
+                    const bool up = (e & k) == 0;
+                    const bool lower = (e & j) == 0;
+                    a[i] = (lower == up) ? fminf(a[i], o) : fmaxf(a[i], o);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if ((i & j) == 0) {
+                        const bool up = ((lane * 4 + i) & k) == 0;
+                        const float x = a[i], y = a[i | j];
+                        a[i] = up ? fminf(x, y) : fmaxf(x, y);
+                        a[i | j] = up ? fmaxf(x, y) : fminf(x, y);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Element e of the sorted warp array (e uniform across the warp).
+__device__ __forceinline__ float sorted_at(const float (&a)[4], int e) {
+    const int i = e & 3;
+    const float v = i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3];
+    return __shfl_sync(0xffffffffu, v, e >> 2);
+}
+
+template <bool kF32>
+__global__ void __launch_bounds__(NUM_THREADS) calib_percentile_kernel(const Params p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float qf = __fdiv_rn(p.p, 100.0f);
+    const float h = __fmul_rn(qf, 127.0f);
+    const float fl = floorf(h);
+    const int lo = min(max(static_cast<int>(fl), 0), 127);
+    const int hi = min(lo + 1, 127);
+    const float f = __fsub_rn(h, fl);
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * WARPS + warp; g < p.groups;
+         g += static_cast<int64_t>(gridDim.x) * WARPS) {
+        float w[4], a[4];
+        load_group4<kF32>(p.W, g, lane, w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = fabsf(w[i]);
+        bitonic128(a, lane);
+        const float alo = sorted_at(a, lo), ahi = sorted_at(a, hi);
+        const float r = __fadd_rn(alo, __fmul_rn(f, __fsub_rn(ahi, alo)));
+        const float s = (r == 0.0f) ? 1.0f : __fdiv_rn(r, 7.0f);
+        store_group(p, g, lane, w, s);
+    }
+}
+
+__device__ __forceinline__ float candidate(int i, int n, float lo, float hi, float step) {
+    if (n == 1) return lo;
+    if (i == n - 1) return hi;
+    return __fadd_rn(lo, __fmul_rn(static_cast<float>(i), step));
+}
+
+template <bool kF32>
+__global__ void __launch_bounds__(NUM_THREADS) calib_mse_kernel(const Params p) {
+    __shared__ __align__(16) float sw[WARPS][128];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4 *sw4 = reinterpret_cast<const float4 *>(sw[warp]);
+    const int n = p.n;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * WARPS + warp; g < p.groups;
+         g += static_cast<int64_t>(gridDim.x) * WARPS) {
+        float w[4];
+        load_group4<kF32>(p.W, g, lane, w);
+        reinterpret_cast<float4 *>(sw[warp])[lane] = make_float4(w[0], w[1], w[2], w[3]);
+        float lo = fminf(fminf(fabsf(w[0]), fabsf(w[1])), fminf(fabsf(w[2]), fabsf(w[3])));
+        float hi = fmaxf(fmaxf(fabsf(w[0]), fabsf(w[1])), fmaxf(fabsf(w[2]), fabsf(w[3])));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        __syncwarp();
+        const float step = n > 1 ? __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(n - 1)) : 0.0f;
+        float best = __int_as_float(0x7f800000);   // +inf
+        int bi = INT_MAX;
+        for (int i = lane; i < n; i += 32) {
+            const float c = candidate(i, n, lo, hi, step);
+            if (c < 1e-10f) continue;
+            float e = 0.0f;
+#pragma unroll 4
+            for (int k4 = 0; k4 < 32; ++k4) {
+                const float4 v = sw4[k4];
+                const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float t = fminf(fmaxf(rintf(__fdiv_rn(x[u], c)), -7.0f), 7.0f);
+                    const float d = __fsub_rn(__fmul_rn(t, c), x[u]);
+                    e = __fadd_rn(e, __fmul_rn(d, d));
+                }
+            }
+            const float mse = __fdiv_rn(e, 128.0f);
+            if (mse < best) {
+                best = mse;
+                bi = i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ob < best || (ob == best && oi < bi)) {
+                best = ob;
+                bi = oi;
+            }
+        }
+        const float s = (bi == INT_MAX) ? 1e-8f : candidate(bi, n, lo, hi, step);
+        store_group(p, g, lane, w, s);
+        __syncwarp();
+    }
+}
+
+}  // namespace calib
+}  // namespace w4

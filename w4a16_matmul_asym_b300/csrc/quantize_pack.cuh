@@ -321,6 +321,7 @@ __global__ void __launch_bounds__(quant::NUM_THREADS, 1)
         prefetch_tensormap(&tmW);
     }
     __syncthreads();
+    pdl_wait_then_release();   // no global memory is touched before this point
 
     if (warp == CW) {
         // ---------------- producer ----------------

@@ -9,6 +9,7 @@
 #include <mutex>
 #include <utility>
 
+#include "act_quant.cuh"
 #include "common.cuh"
 #include "dequantize.cuh"
 #include "gemm_tcgen05.cuh"
@@ -16,6 +17,7 @@
 #include "gemv_dp4a.cuh"
 #include "gemv_mma.cuh"
 #include "gemv_tc.cuh"
+#include "gptq.cuh"
 #include "quantize_calib.cuh"
 #include "quantize_pack.cuh"
 
@@ -64,6 +66,25 @@ int launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+// As launch(), with programmatic dependent launch: the kernel may begin launching while
+// the previous kernel in the stream finishes; it must execute griddepcontrol.wait before
+// touching global memory.
+template <typename Kern, typename... Args>
+int launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
@@ -157,11 +178,11 @@ int launch_gemv_dp4a(const __nv_bfloat16 *A, int64_t N, int64_t K, const uint8_t
     if (H == 1) {
         auto kern = gd::w4a16_gemv_dp4a_kernel<1>;
         if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
-        return launch(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
+        return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
     }
     auto kern = gd::w4a16_gemv_dp4a_kernel<2>;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
-    return launch(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
 }
 
 // 2 <= M <= 16 on the tensor cores: K a multiple of 2048, the activations (M x K bf16)
@@ -211,31 +232,36 @@ int launch_skinny_tc(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, co
 }
 
 // 1 <= M <= 16 on warp-level tensor-core MMAs with the weights dequantized in
-// registers: K a multiple of 2048, 16-byte aligned scale and zero-point tables, the
-// activations (M x K bf16) resident in shared memory next to at least two stages.
-// Returns W4_ERR_UNSUPPORTED for other shapes.
-int launch_gemv_mma(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const uint8_t *qweight,
-                    const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y, cudaStream_t stream,
-                    int sms, w4::WaitParams wp) {
+// registers: K a multiple of 2048, the activations (M x K bf16 after widening) resident
+// in shared memory next to at least two stages.  Scale and zero-point tables must be
+// 16-byte aligned (W4_ERR_MISALIGNED otherwise when `strict`, else UNSUPPORTED so the
+// caller can pick another kernel).  Returns W4_ERR_UNSUPPORTED for other shapes.
+// A is bf16, or int8 when i8 (W4A8); row_scale (may be null) multiplies output row m.
+bool gemv_mma_shape_ok(int64_t M, int64_t K) {
     namespace gm = w4::gmma;
-    if (M < 1 || M > 16 || K % gm::KC != 0 || K > (int64_t(1) << 20) || !aligned(scales, 16) ||
-        !aligned(zeros, 16) || N > INT32_MAX / 2)
-        return W4_ERR_UNSUPPORTED;
+    if (M < 1 || M > 16 || K % gm::k_per_stage(1) != 0 || K > (int64_t(1) << 20)) return false;
+    int gpw = 0, stages = 0;
+    gm::plan(static_cast<int>(M), static_cast<int>(K), &gpw, &stages);
+    return stages > 0;
+}
+
+int launch_gemv_mma(const void *A, bool i8, const float *row_scale, int64_t M, int64_t N, int64_t K,
+                    const uint8_t *qweight, const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y,
+                    cudaStream_t stream, int sms, w4::WaitParams wp, bool strict) {
+    namespace gm = w4::gmma;
+    if (!gemv_mma_shape_ok(M, K) || N > INT32_MAX / 2) return W4_ERR_UNSUPPORTED;
+    if (!aligned(scales, 16) || !aligned(zeros, 16)) return strict ? W4_ERR_MISALIGNED : W4_ERR_UNSUPPORTED;
     const int m = static_cast<int>(M), k = static_cast<int>(K);
     const int nb = m <= 8 ? 1 : 2;
-    int stages = 0;
-    for (int s = gm::MAX_STAGES; s >= 2; --s)
-        if (gm::smem_bytes(m, k, nb, s) <= gm::SMEM_LIMIT) {
-            stages = s;
-            break;
-        }
-    if (stages == 0) return W4_ERR_UNSUPPORTED;
-    const int smem = gm::smem_bytes(m, k, nb, stages);
+    int gpw = 0, stages = 0;
+    gm::plan(m, k, &gpw, &stages);
+    const int smem = gm::smem_bytes(m, k, nb, gpw, stages);
     gm::Params prm;
     prm.A = A;
     prm.qweight = qweight;
     prm.scales = scales;
     prm.zeros = zeros;
+    prm.row_scale = row_scale;
     prm.Y = Y;
     prm.M = m;
     prm.N = static_cast<int>(N);
@@ -245,10 +271,13 @@ int launch_gemv_mma(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, con
     prm.wait = wp;
     const int grid = prm.tiles < sms ? prm.tiles : sms;
     CUtensorMap tmW, tmS, tmZ;
-    if (!gm::make_maps(&tmW, &tmS, &tmZ, qweight, scales, zeros, N, K)) return W4_ERR_CUDA;
-    auto kern = nb == 1 ? gm::gemv_mma_kernel<1> : gm::gemv_mma_kernel<2>;
+    if (!gm::make_maps(&tmW, &tmS, &tmZ, qweight, scales, zeros, N, K, gpw)) return W4_ERR_CUDA;
+    decltype(&gm::gemv_mma_kernel<1, 1, false>) kern;
+    if (nb == 1 && gpw == 2) kern = i8 ? gm::gemv_mma_kernel<1, 2, true> : gm::gemv_mma_kernel<1, 2, false>;
+    else if (nb == 1) kern = i8 ? gm::gemv_mma_kernel<1, 1, true> : gm::gemv_mma_kernel<1, 1, false>;
+    else kern = i8 ? gm::gemv_mma_kernel<2, 1, true> : gm::gemv_mma_kernel<2, 1, false>;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
-    return launch(kern, dim3(grid), dim3(gm::NUM_THREADS), smem, stream, tmW, tmS, tmZ, prm);
+    return launch_pdl(kern, dim3(grid), dim3(gm::NUM_THREADS), smem, stream, tmW, tmS, tmZ, prm);
 }
 
 // M <= 8.  The streaming kernels need the scales / zero points reachable by 2-D tensor
@@ -362,11 +391,11 @@ int quantize_pack_impl(const void *W, int w_dtype, int64_t N, int64_t K, int gro
     if (w_dtype == W4_DTYPE_F16) {
         auto kern = w4::quantize_pack_kernel<false, kSym>;
         if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
-        return launch(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
+        return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
     }
     auto kern = w4::quantize_pack_kernel<true, kSym>;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
-    return launch(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
+    return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
 }
 
 // Both calibrated quantizers: validation and the launch (one warp per group).
@@ -492,7 +521,8 @@ int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const u
     // whenever K is a multiple of 2048 and the activations fit in shared memory.  (M = 1
     // stays on the integer-dot GEMV, faster there: 8.3 against 11.7 us on 11008 x 4096.)
     if (M >= 2 && M <= 16) {
-        const int rc = launch_gemv_mma(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
+        const int rc = launch_gemv_mma(a, false, nullptr, M, N, K, qweight, s, zeros, y, stream, sms, wait_params(),
+                                       false);
         if (rc != W4_ERR_UNSUPPORTED) return rc;
     }
     // 9 <= M <= 16 with few 128-row tiles: the GEMM would leave SMs idle, while the
@@ -505,6 +535,93 @@ int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const u
     }
     if (M <= 8) return launch_gemv(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
     return w4::launch_gemm_tcgen05(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
+}
+
+int w4_quantize_act_int8(const void *A, int64_t M, int64_t K, int8_t *a_q, float *a_scale, cudaStream_t stream) {
+    if (M < 0 || K < 0 || K % 8 != 0) return W4_ERR_INVALID_ARG;
+    if (M == 0) return W4_OK;
+    if (!a_scale || (K > 0 && (!A || !a_q))) return W4_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(a_q, 16) || !aligned(a_scale, 4)) return W4_ERR_MISALIGNED;
+    if (M > INT64_MAX / (K > 0 ? K : 1)) return W4_ERR_INVALID_ARG;
+    int sms = 0;
+    if (int rc = current_sm_count(&sms)) return rc;
+    namespace aq = w4::actq;
+    int64_t blocks = (M + aq::WARPS - 1) / aq::WARPS;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    return launch(aq::act_quant_int8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(aq::NUM_THREADS), 0, stream,
+                  static_cast<const __nv_bfloat16 *>(A), M, K, a_q, a_scale);
+}
+
+size_t w4_matmul_w4a8_workspace_size(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0 || gemv_mma_shape_ok(M, K)) return 0;
+    if (M > INT64_MAX / 2 / K) return 0;
+    return static_cast<size_t>((M * K * 2 + 255) / 256 * 256);
+}
+
+int w4_matmul_w4a8(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N, int64_t K, int group,
+                   const uint8_t *qweight, const void *scales, const uint8_t *zeros, void *Y, void *workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || group <= 0) return W4_ERR_INVALID_ARG;
+    if (group != W4_GROUP_SIZE) return W4_ERR_UNSUPPORTED;
+    if (K % group != 0) return W4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!Y) return W4_ERR_INVALID_ARG;
+    if (!aligned(Y, 2)) return W4_ERR_MISALIGNED;
+    if (K == 0) {
+        const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(M * N) * 2, stream);
+        return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+    }
+    if (!a_q || !a_scale || !qweight || !scales || !zeros) return W4_ERR_INVALID_ARG;
+    if (!aligned(a_q, 16) || !aligned(a_scale, 4) || !aligned(qweight, 16) || !aligned(scales, 2))
+        return W4_ERR_MISALIGNED;
+    int sms = 0;
+    if (int rc = current_sm_count(&sms)) return rc;
+    const __half *s = static_cast<const __half *>(scales);
+    __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(Y);
+    if (gemv_mma_shape_ok(M, K))   // decode shapes: widened while staged, no workspace
+        return launch_gemv_mma(a_q, true, a_scale, M, N, K, qweight, s, zeros, y, stream, sms, wait_params(), true);
+    // Other shapes: a_q widened (exactly) to bf16 in the workspace, then the tcgen05 GEMM
+    // with the per-row activation scale applied in its epilogue.
+    const size_t need = w4_matmul_w4a8_workspace_size(M, K);
+    if (!workspace || workspace_bytes < need) return W4_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return W4_ERR_MISALIGNED;
+    __nv_bfloat16 *abf = static_cast<__nv_bfloat16 *>(workspace);
+    const int64_t n8 = M * K / 8;
+    int64_t blocks = (n8 + 255) / 256;
+    if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
+    if (int rc = launch(w4::actq::int8_to_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a_q,
+                        abf, n8))
+        return rc;
+    return w4::launch_gemm_tcgen05(abf, M, N, K, qweight, s, zeros, y, stream, sms, wait_params(), a_scale);
+}
+
+int w4_gptq_quantize(const void *W, int w_dtype, int64_t N, int64_t K, int group, const float *U,
+                     uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream) {
+    if (N < 0 || K < 0 || group <= 0) return W4_ERR_INVALID_ARG;
+    if (w_dtype != W4_DTYPE_F16 && w_dtype != W4_DTYPE_F32) return W4_ERR_INVALID_ARG;
+    if (group != W4_GROUP_SIZE) return W4_ERR_UNSUPPORTED;
+    if (K % group != 0) return W4_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return W4_OK;
+    if (K > 8192 || N > INT32_MAX / 2) return W4_ERR_UNSUPPORTED;
+    if (!W || !U || !qweight || !scales || !zeros) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(U, 16) || !aligned(qweight, 16) || !aligned(scales, 2))
+        return W4_ERR_MISALIGNED;
+    namespace gq = w4::gptq;
+    gq::Params prm;
+    prm.W = W;
+    prm.U = U;
+    prm.qweight = qweight;
+    prm.scales = static_cast<__half *>(scales);
+    prm.zeros = zeros;
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.R = gq::rows_for(prm.K);
+    const int smem = gq::smem_bytes(prm.K, prm.R);
+    const int64_t grid = (N + prm.R - 1) / prm.R;
+    auto kern = w_dtype == W4_DTYPE_F32 ? gq::gptq_kernel<true> : gq::gptq_kernel<false>;
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
+    return launch(kern, dim3(static_cast<unsigned>(grid)), dim3(gq::NUM_THREADS), smem, stream, prm);
 }
 
 int w4_check_device_error(cudaStream_t stream) {
