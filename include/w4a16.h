@@ -265,10 +265,13 @@ W4_API int w4_quantize_act_int8(const void *A, int64_t M, int64_t K, int8_t *a_q
  * Per-Channel Scale" (Step 5, forward_quant: the INT8 activations times their per-token
  * scale, multiplied by the dequantized INT4 weights).  Accuracy contract per element:
  *     |Y - Y_exact| <= 8e-3 * sum_k |a_q[m,k] a_scale[m] W_hat[n,k]| + ulp_bf16(|Y_exact|) / 2.
- * The int8 x int4 products are exact in bf16 x bf16 -> fp32, so the contraction runs on
- * the bf16 tensor pipe (this part's int8 tensor rate is far below its bf16 rate):
- *   1 <= M <= 16, K a multiple of 2048 (activations fitting in shared memory): the
- *     decode kernel of w4_matmul, a_q widened to bf16 while staged; no workspace.
+ * Paths, none of them using the int8 tensor pipe (this part's int8 tensor rate is far
+ * below its bf16 rate):
+ *   M = 1, K a multiple of 2048 up to 16384: integer dot products (dp4a) of the int8
+ *     activations with the 4-bit levels, exact in int32 per group; no workspace.
+ *   1 <= M <= 16 otherwise, K a multiple of 2048 (activations fitting in shared memory):
+ *     the decode kernel of w4_matmul, a_q widened to bf16 while staged (int8 x int4
+ *     products are exact in bf16 x bf16 -> fp32); no workspace.
  *   otherwise: a_q is widened to bf16 into `workspace` and the tcgen05 GEMM of w4_matmul
  *     runs with a_scale applied to each output row before rounding.
  *

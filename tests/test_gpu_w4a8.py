@@ -77,10 +77,13 @@ def run_w4a8(env, A_bits, W, M):
     return Yb, (aq, sa, q, s, z)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 300, 2048), (2, 37, 4096), (8, 1031, 8192), (16, 200, 4096),
+@pytest.mark.parametrize("M,N,K", [(1, 300, 2048), (1, 1031, 4096), (1, 77, 8192), (1, 5000, 16384),
+                                   (2, 37, 4096), (8, 1031, 8192), (16, 200, 4096),
                                    (5, 17, 6144), (12, 2500, 2048)])
 def test_w4a8_decode_path(env, M, N, K):
-    """Shapes the decode kernel takes: int8 widened while staged, no workspace."""
+    """Shapes the decode kernels take, with no workspace: M = 1 on integer dot products
+    over the int8 digits (half-group, one-group and two-warp-per-row layouts), larger M
+    on the warp-MMA kernel with the int8 activations widened while staged."""
     import synth
     torch, w4, orc = env
     assert w4.w4_matmul_w4a8_workspace_size(M, K) == 0
@@ -124,6 +127,23 @@ def test_w4a8_prefill_workload_sampled(env):
     mi, ni = rng.integers(0, A.shape[0], 4000), rng.integers(0, W.shape[0], 4000)
     Yref, S = orc.w4a8_matmul_entries(aq, sa, q, s, z, mi, ni)
     ok, worst, idx = orc.check_y(Yb[mi, ni], Yref, S)
+    assert ok, (worst, idx)
+
+
+@pytest.mark.parametrize("name", ["llama7b_gemv", "mlp70b"])
+def test_w4a8_decode_full_workloads(env, name):
+    """The M = 1 decode workloads at full size through the GPU activation quantizer and
+    the W4A8 decode kernel, every output compared."""
+    import synth
+    torch, w4, orc = env
+    W, A = synth.make_workload(name)
+    q, s, z = orc.quantize_pack(W)
+    aqd, sad = w4.quantize_act_int8(to_dev_bf16(torch, A))
+    Y = w4.matmul_w4a8(aqd, sad, torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda())
+    torch.cuda.synchronize()
+    aq, sa = aqd.cpu().numpy(), sad.cpu().numpy()
+    Yref, S = orc.w4a8_matmul(aq, sa, q, s, z)
+    ok, worst, idx = orc.check_y(Y.view(torch.int16).cpu().numpy().view(np.uint16), Yref, S)
     assert ok, (worst, idx)
 
 

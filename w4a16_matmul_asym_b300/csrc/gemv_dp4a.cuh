@@ -38,6 +38,12 @@
 //                bf16 rounding and a coalesced store of y.
 // Every wait is bounded (common.cuh); after a timeout the CTA drains its copies and
 // exits with W4_ERR_TIMEOUT recorded.
+//
+// W4A8 ("Hands-On Build Guide: Group-Wise INT4 Weight-Only Quantization with
+// Per-Channel Scale", Step 5): with int8 activations (I8) the digits are the activations
+// themselves, one signed byte per level, so the conversion reduces to a byte permute,
+// there are no residuals, two dp4a cover 8 levels, and the epilogue multiplies the
+// row's sum by the token's activation scale before rounding.
 #pragma once
 
 #include "common.cuh"
@@ -55,7 +61,8 @@ constexpr int RS = 4;                      // reduction slots
 constexpr int SMEM_LIMIT = 227 * 1024;
 
 struct Params {
-    const __nv_bfloat16 *A;
+    const void *A;     // bf16 [K], or int8 [K] (I8)
+    const float *row_scale;  // I8: the activation scale a_scale[0]
     const uint8_t *qweight;
     const __half *scales;
     const uint8_t *zeros;
@@ -143,7 +150,7 @@ __device__ __forceinline__ int lane_rot(int l) {
     return H == 1 ? ((l >> 1) & 3) : ((l >> 2) & 1);
 }
 
-template <int H>
+template <int H, bool I8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const Params p) {
     constexpr int WP = Layout<H>::WP;
     constexpr int NCH = WP / 4;                    // 32-level chunks per lane
@@ -199,8 +206,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
 #pragma unroll
             for (int s = 0; s < MAX_STAGES; ++s) issued_parity[s] = -1;
             bool ok = true;
-            mbar_arrive_expect_tx(a_bar, static_cast<uint32_t>(K) * 2);
-            bulk_copy_g2s(res, p.A, static_cast<uint32_t>(K) * 2, a_bar, policy_evict_last());
+            const uint32_t a_bytes = static_cast<uint32_t>(K) * (I8 ? 1u : 2u);
+            mbar_arrive_expect_tx(a_bar, a_bytes);
+            bulk_copy_g2s(res, p.A, a_bytes, a_bar, policy_evict_last());
             for (int lt = 0; lt < num_stages; ++lt) {
                 const int stage = lt % S;
                 const uint32_t phase = static_cast<uint32_t>(lt / S) & 1u;
@@ -245,7 +253,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
         const int nconv = (CW + 1) * 32;
         const int cw_id = warp < CW ? warp : CW;   // epilogue warp takes the last slot
         const bool have_a = warp_wait_full_bounded(a_bar, 0, abort_flag, tmo);
-        for (int base = cw_id * 32; have_a && base < K / 16; base += nconv) {
+        for (int base = cw_id * 32; I8 && have_a && base < K / 16; base += nconv) {
+            // int8 activations: the digit words are byte permutes (levels 0 2 4 6 and
+            // 1 3 5 7 of each packed word), one signed digit, no residuals.
+            const int sg = base + lane;
+            const bool act = sg < K / 16;
+            const uint4 x = act ? reinterpret_cast<const uint4 *>(res)[sg] : make_uint4(0, 0, 0, 0);
+            uint32_t dw[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}};
+            dw[0][0] = byte_perm(x.x, x.y, 0x6420u);
+            dw[0][3] = byte_perm(x.x, x.y, 0x7531u);
+            dw[1][0] = byte_perm(x.z, x.w, 0x6420u);
+            dw[1][3] = byte_perm(x.z, x.w, 0x7531u);
+            int vsum = 0;
+            const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vsum = __dp4a(static_cast<int>(xw[i]), 0x01010101, vsum);
+            const int g = sg >> 3;
+            const int piece = g * H + (sg & 7) / (8 / H);
+            const int wi = ((sg & 7) % (8 / H)) * 2;
+            const int l = piece & 31;
+            const int cpos = wi >> 2;
+            const int slot = (cpos - lane_rot<H>(l)) & (NCH - 1);
+#pragma unroll
+            for (int o = 1; o < 8 / H; o <<= 1) vsum += __shfl_xor_sync(0xffffffffu, vsum, o);
+            if (act) {
+                uint4 *dst = reinterpret_cast<uint4 *>(dig + piece * PAD + (slot * 4 + (wi & 3)) * 6);
+                dst[0] = make_uint4(dw[0][0], dw[0][1], dw[0][2], dw[0][3]);
+                dst[1] = make_uint4(dw[0][4], dw[0][5], dw[1][0], dw[1][1]);
+                dst[2] = make_uint4(dw[1][2], dw[1][3], dw[1][4], dw[1][5]);
+                if ((sg & 1) == 0) cmask[sg >> 1] = 0u;
+                if ((sg & 7) % (8 / H) == 0) svs[piece] = vsum;
+                if ((sg & 7) == 0) cscs[g] = 1.0f;
+            }
+        }
+        for (int base = cw_id * 32; !I8 && have_a && base < K / 16; base += nconv) {
             const int sg = base + lane;            // 16-level segment; K / 16 is a multiple of 8
             const bool act = sg < K / 16;
             uint32_t w[8];                         // 16 bf16, two per word, natural order
@@ -441,12 +482,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
                     for (int w = 0; w < 4; ++w) {
                         const uint32_t ev = x[w] & 0x0F0F0F0Fu;
                         const uint32_t od = (x[w] >> 4) & 0x0F0F0F0Fu;
-                        s0e[i] = dp4a_uu(dg[j][w][0], ev, s0e[i]);
-                        s1e[i] = dp4a_uu(dg[j][w][1], ev, s1e[i]);
-                        s2e[i] = dp4a_su(dg[j][w][2], ev, s2e[i]);
-                        s0o[i] = dp4a_uu(dg[j][w][3], od, s0o[i]);
-                        s1o[i] = dp4a_uu(dg[j][w][4], od, s1o[i]);
-                        s2o[i] = dp4a_su(dg[j][w][5], od, s2o[i]);
+                        if constexpr (I8) {        // one signed digit
+                            s2e[i] = dp4a_su(dg[j][w][0], ev, s2e[i]);
+                            s2o[i] = dp4a_su(dg[j][w][3], od, s2o[i]);
+                        } else {
+                            s0e[i] = dp4a_uu(dg[j][w][0], ev, s0e[i]);
+                            s1e[i] = dp4a_uu(dg[j][w][1], ev, s1e[i]);
+                            s2e[i] = dp4a_su(dg[j][w][2], ev, s2e[i]);
+                            s0o[i] = dp4a_uu(dg[j][w][3], od, s0o[i]);
+                            s1o[i] = dp4a_uu(dg[j][w][4], od, s1o[i]);
+                            s2o[i] = dp4a_su(dg[j][w][5], od, s2o[i]);
+                        }
                     }
                 }
             }
@@ -489,8 +535,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
             for (int i = 0; i < RB; ++i) {
                 const int r = rb * RB + i;
                 // sum_k v_k (q_k - zp); intermediate values wrap, the result fits in int32.
-                const uint32_t tu = static_cast<uint32_t>(s2e[i] + s2o[i]) * 65536u + (s1e[i] + s1o[i]) * 256u +
-                                    (s0e[i] + s0o[i]) - zp[i] * static_cast<uint32_t>(sv);
+                const uint32_t tu = I8 ? static_cast<uint32_t>(s2e[i] + s2o[i]) - zp[i] * static_cast<uint32_t>(sv)
+                                       : static_cast<uint32_t>(s2e[i] + s2o[i]) * 65536u + (s1e[i] + s1o[i]) * 256u +
+                                             (s0e[i] + s0o[i]) - zp[i] * static_cast<uint32_t>(sv);
                 float part = __fmul_rn(__fmul_rn(__int2float_rn(static_cast<int>(tu)), sf[i]), csc);
                 part = __fmaf_rn(sf[i], rr[i], part);
                 rd[r * red_stride + piece] = active ? part : 0.0f;
@@ -523,6 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
             if (r < rows) {
                 float y = 0.0f;
                 for (int j = 0; j < 32 * WR; ++j) y += rd[r * red_stride + j];
+                if constexpr (I8) y = __fmul_rn(y, p.row_scale[0]);
                 p.Y[r0 + r] = __float2bfloat16_rn(y);
             }
             __syncwarp();

@@ -413,6 +413,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t chunk = static_cast<uint32_t>(((warp & 1) * 4 + t4) ^ (r0 & 7)) << 4;
     const uint32_t w_off0 = (warp >> 1) * (ROWS * PAIR_BYTES) + r0 * PAIR_BYTES + chunk;
     constexpr uint32_t W_J = 8 * ROWS * PAIR_BYTES;   // offset of group w + 16 from group w
+    // Scale / zero-point offsets within a stage, and the B-fragment addresses: chunk
+    // ((4 g + v) M + m) 4 + t with g = GPS ks + warp + 16 h, so every address is a fixed
+    // per-lane base plus (ks, h, v, nb) multiples of compile-time or loop-invariant strides.
+    const uint32_t s_off0 = r0 * (GPS * 2) + warp * 2, s_off1 = r1 * (GPS * 2) + warp * 2;
+    const uint32_t z_off0 = SS + r0 * GPS + warp, z_off1 = SS + r1 * GPS + warp;
+    const uint32_t b_row = 64u * M;                        // bytes from (g, v) to (g, v + 1)
+    const uint32_t b_lane = a_base + ((warp * 4 * M + g8) * 4 + t4) * 16;
+    const uint32_t b_stage = b_row * 4 * GPS;              // bytes per stage of groups
+    bool bvalid[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) bvalid[nb] = g8 + 8 * nb < M;
     float y[NB][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
@@ -420,8 +431,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < 4; ++i) y[nb][i] = 0.0f;
 
     uint32_t slot = 0, phase = 0;
+    int j = 0, ks = 0;                                     // tile within the CTA, stage within the tile
+    uint32_t b_ks = b_lane;
     for (int i = 0; ok && i < nstages; ++i) {
-        const int j = i / KS, ks = i - j * KS;
         if (!warp_wait(&full[slot], phase, abort_flag, tmo, false)) {
             ok = false;
             break;
@@ -431,15 +443,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float sf0[GPW], sf1[GPW];
 #pragma unroll
         for (int h = 0; h < GPW; ++h) {
-            const int gs = warp + CW * h;
             const uint4 w0 = lds128(stw + w_off0 + h * W_J);
             const uint4 w1 = lds128(stw + w_off0 + h * W_J + 8 * PAIR_BYTES);
             wa[h][0] = w0.x; wa[h][1] = w0.y; wa[h][2] = w0.z; wa[h][3] = w0.w;
             wb[h][0] = w1.x; wb[h][1] = w1.y; wb[h][2] = w1.z; wb[h][3] = w1.w;
-            sf0[h] = half_bits_to_f32(lds_u16(stsz + r0 * (GPS * 2) + gs * 2));
-            sf1[h] = half_bits_to_f32(lds_u16(stsz + r1 * (GPS * 2) + gs * 2));
-            zz0[h] = kBf16x2_128 + lds_u8(stsz + SS + r0 * GPS + gs) * 0x00010001u;  // bf16 pair (128 + zp)
-            zz1[h] = kBf16x2_128 + lds_u8(stsz + SS + r1 * GPS + gs) * 0x00010001u;
+            sf0[h] = half_bits_to_f32(lds_u16(stsz + s_off0 + h * (CW * 2)));
+            sf1[h] = half_bits_to_f32(lds_u16(stsz + s_off1 + h * (CW * 2)));
+            zz0[h] = kBf16x2_128 + lds_u8(stsz + z_off0 + h * CW) * 0x00010001u;  // bf16 pair (128 + zp)
+            zz1[h] = kBf16x2_128 + lds_u8(stsz + z_off1 + h * CW) * 0x00010001u;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -461,7 +472,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int v = 0; v < 4; ++v) {
 #pragma unroll
             for (int h = 0; h < GPW; ++h) {
-                const int g = ks * GPS + warp + CW * h;   // group within the row
                 uint32_t pa[4], pb[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -470,9 +480,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
 #pragma unroll
                 for (int nb = 0; nb < NB; ++nb) {
-                    const int m = g8 + 8 * nb;
-                    const uint4 bf = m < M ? lds128(a_base + ((((g * 4 + v) * M + m) * 4 + t4) << 4))
-                                           : make_uint4(0, 0, 0, 0);
+                    // group GPS ks + warp + 16 h, piece v, activation row g8 + 8 nb
+                    const uint4 bf = bvalid[nb] ? lds128(b_ks + (CW * h * 4 + v) * b_row + nb * 512)
+                                                : make_uint4(0, 0, 0, 0);
                     mma_bf16(d[h][nb][0], pa[0], pb[0], pa[1], pb[1], bf.x, bf.y);
                     mma_bf16(d[h][nb][1], pa[2], pb[2], pa[3], pb[3], bf.z, bf.w);
                 }
@@ -488,7 +498,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 y[nb][3] = fmaf(sf1[h], __fadd_rn(d[h][nb][0][3], d[h][nb][1][3]), y[nb][3]);
             }
 
-        if (ks == KS - 1) {  // tile done: partial sums to the reduction area
+        b_ks += b_stage;
+        if (++ks == KS) {  // tile done: partial sums to the reduction area
+            ks = 0;
+            b_ks = b_lane;
             const int b = j & 1;
             if (!warp_wait(&red_empty[b], static_cast<uint32_t>(((j >> 1) & 1) ^ 1), abort_flag, tmo, false)) {
                 ok = false;
@@ -507,6 +520,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&red_full[b]);
+            ++j;
         }
     }
 }

@@ -22,12 +22,15 @@
 // Mapping: one warp per group, lane l holding elements 4l .. 4l+3; a grid-stride loop
 // over the flat group index G (W elements [128 G, 128 G + 128), qweight bytes
 // [64 G, 64 G + 64), scales[G], zeros[G]).
-//   percentile: the warp sorts the 128 magnitudes with a bitonic network (registers and
-//     xor-shuffles) and reads the two order statistics it needs.
+//   percentile: the two order statistics it needs are found by repeated warp max- (or
+//     min-) extraction when they lie within 8 of the top (or bottom) -- the usual
+//     p = 99.9 takes two rounds -- and otherwise by a bitonic sort of the 128 magnitudes
+//     (registers and xor-shuffles).  Either way the values are exact order statistics.
 //   mse: the group goes to shared memory; lane l scores candidates l, l + 32, ... over
 //     all 128 elements (broadcast reads), keeping its first minimum; a warp reduction
 //     takes the smallest score, ties to the lower candidate index.  This is ALU work:
-//     n * 128 quotients per group.
+//     n * 128 quotients per group, each rounded from a reciprocal product except near a
+//     tie (where the IEEE quotient is computed), which gives the same integer.
 #pragma once
 
 #include <climits>
@@ -120,6 +123,29 @@ __device__ __forceinline__ float sorted_at(const float (&a)[4], int e) {
     return __shfl_sync(0xffffffffu, v, e >> 2);
 }
 
+// The largest (kMax) or smallest remaining value of the warp's 128, returned to every
+// lane, and one instance of it removed (the lowest lane, then the lowest register, that
+// holds it; removed values become a sentinel outside [0, inf)).  Magnitudes only.
+template <bool kMax>
+__device__ __forceinline__ float extract(float (&a)[4], int lane) {
+    const float sentinel = kMax ? -1.0f : __int_as_float(0x7f800000);
+    float m = kMax ? fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) : fminf(fminf(a[0], a[1]), fminf(a[2], a[3]));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float t = __shfl_xor_sync(0xffffffffu, m, o);
+        m = kMax ? fmaxf(m, t) : fminf(m, t);
+    }
+    const bool has = (a[0] == m) | (a[1] == m) | (a[2] == m) | (a[3] == m);
+    const int owner = __ffs(__ballot_sync(0xffffffffu, has)) - 1;
+    if (lane == owner) {
+        if (a[0] == m) a[0] = sentinel;
+        else if (a[1] == m) a[1] = sentinel;
+        else if (a[2] == m) a[2] = sentinel;
+        else a[3] = sentinel;
+    }
+    return m;
+}
+
 template <bool kF32>
 __global__ void __launch_bounds__(NUM_THREADS) calib_percentile_kernel(const Params p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,8 +161,26 @@ __global__ void __launch_bounds__(NUM_THREADS) calib_percentile_kernel(const Par
         load_group4<kF32>(p.W, g, lane, w);
 #pragma unroll
         for (int i = 0; i < 4; ++i) a[i] = fabsf(w[i]);
-        bitonic128(a, lane);
-        const float alo = sorted_at(a, lo), ahi = sorted_at(a, hi);
+        float alo, ahi;
+        if (lo >= 120) {                      // from the top: round r gives a_(127 - r)
+            alo = ahi = 0.0f;
+            for (int r = 0; r <= 127 - lo; ++r) {
+                const float v = extract<true>(a, lane);
+                if (r == 127 - hi) ahi = v;
+                if (r == 127 - lo) alo = v;
+            }
+        } else if (hi <= 7) {                 // from the bottom: round r gives a_r
+            alo = ahi = 0.0f;
+            for (int r = 0; r <= hi; ++r) {
+                const float v = extract<false>(a, lane);
+                if (r == lo) alo = v;
+                if (r == hi) ahi = v;
+            }
+        } else {
+            bitonic128(a, lane);
+            alo = sorted_at(a, lo);
+            ahi = sorted_at(a, hi);
+        }
         const float r = __fadd_rn(alo, __fmul_rn(f, __fsub_rn(ahi, alo)));
         const float s = (r == 0.0f) ? 1.0f : __fdiv_rn(r, 7.0f);
         store_group(p, g, lane, w, s);
@@ -174,6 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS) calib_mse_kernel(const Params p) 
         for (int i = lane; i < n; i += 32) {
             const float c = candidate(i, n, lo, hi, step);
             if (c < 1e-10f) continue;
+            const float rc = __frcp_rn(c);          // finite: c >= 1e-10
             float e = 0.0f;
 #pragma unroll 4
             for (int k4 = 0; k4 < 32; ++k4) {
@@ -181,7 +226,14 @@ __global__ void __launch_bounds__(NUM_THREADS) calib_mse_kernel(const Params p) 
                 const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float t = fminf(fmaxf(rintf(__fdiv_rn(x[u], c)), -7.0f), 7.0f);
+                    // rint of the IEEE quotient: from x * fl(1/c) (within 3 ulp of it)
+                    // unless that lies within 2^-16 of a half-integer (or is not
+                    // finite), where the quotient itself is taken.  Beyond |x| = 7.5 the
+                    // clamp makes both give +-7.
+                    const float xr = __fmul_rn(x[u], rc);
+                    float r = rintf(xr);
+                    if (!(fabsf(__fsub_rn(xr, r)) < 0.4999847412109375f)) r = rintf(__fdiv_rn(x[u], c));
+                    const float t = fminf(fmaxf(r, -7.0f), 7.0f);
                     const float d = __fsub_rn(__fmul_rn(t, c), x[u]);
                     e = __fadd_rn(e, __fmul_rn(d, d));
                 }

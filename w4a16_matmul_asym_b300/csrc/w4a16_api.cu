@@ -137,7 +137,7 @@ constexpr size_t kGemvSmemLimit = 220 * 1024;
 
 // M = 1 on integer dot products: K a multiple of 2048 up to 16384, 16-byte aligned
 // scales and zero points.  Returns W4_ERR_UNSUPPORTED for other shapes.
-int launch_gemv_dp4a(const __nv_bfloat16 *A, int64_t N, int64_t K, const uint8_t *qweight,
+int launch_gemv_dp4a(const void *A, bool i8, const float *row_scale, int64_t N, int64_t K, const uint8_t *qweight,
                      const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y, cudaStream_t stream,
                      int sms, w4::WaitParams wp) {
     namespace gd = w4::gemv_dp4a;
@@ -162,6 +162,7 @@ int launch_gemv_dp4a(const __nv_bfloat16 *A, int64_t N, int64_t K, const uint8_t
     if (stages == 0) return W4_ERR_UNSUPPORTED;
     gd::Params prm;
     prm.A = A;
+    prm.row_scale = row_scale;
     prm.qweight = qweight;
     prm.scales = scales;
     prm.zeros = zeros;
@@ -175,12 +176,8 @@ int launch_gemv_dp4a(const __nv_bfloat16 *A, int64_t N, int64_t K, const uint8_t
     const int64_t per_cta = (N + grid - 1) / grid;
     grid = (N + per_cta - 1) / per_cta;
     prm.rows_per_cta = static_cast<int>(per_cta);
-    if (H == 1) {
-        auto kern = gd::w4a16_gemv_dp4a_kernel<1>;
-        if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
-        return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
-    }
-    auto kern = gd::w4a16_gemv_dp4a_kernel<2>;
+    auto kern = H == 1 ? (i8 ? gd::w4a16_gemv_dp4a_kernel<1, true> : gd::w4a16_gemv_dp4a_kernel<1, false>)
+                       : (i8 ? gd::w4a16_gemv_dp4a_kernel<2, true> : gd::w4a16_gemv_dp4a_kernel<2, false>);
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
 }
@@ -289,7 +286,7 @@ int launch_gemv(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const u
                 cudaStream_t stream, int sms, w4::WaitParams wp) {
     namespace gv = w4::gemv;
     if (M == 1) {
-        const int rc = launch_gemv_dp4a(A, N, K, qweight, scales, zeros, Y, stream, sms, wp);
+        const int rc = launch_gemv_dp4a(A, false, nullptr, N, K, qweight, scales, zeros, Y, stream, sms, wp);
         if (rc != W4_ERR_UNSUPPORTED) return rc;
     }
     const int64_t ng = K / 128;
@@ -579,6 +576,10 @@ int w4_matmul_w4a8(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N
     if (int rc = current_sm_count(&sms)) return rc;
     const __half *s = static_cast<const __half *>(scales);
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(Y);
+    if (M == 1) {                  // one token: integer dot products on the int8 digits
+        const int rc = launch_gemv_dp4a(a_q, true, a_scale, N, K, qweight, s, zeros, y, stream, sms, wait_params());
+        if (rc != W4_ERR_UNSUPPORTED) return rc;
+    }
     if (gemv_mma_shape_ok(M, K))   // decode shapes: widened while staged, no workspace
         return launch_gemv_mma(a_q, true, a_scale, M, N, K, qweight, s, zeros, y, stream, sms, wait_params(), true);
     // Other shapes: a_q widened (exactly) to bf16 in the workspace, then the tcgen05 GEMM
