@@ -15,12 +15,15 @@
  *
  * Ownership: the caller allocates and owns every buffer (including the scratch
  * workspace w4_matmul_w4a8 may ask for); the library allocates no device or host
- * memory, keeps no per-call state, and holds no pointer after return.
+ * memory, keeps no per-call state, and holds no pointer after return.  The one
+ * exception is the fixed scratch array of w4_matmul_w4a8_noalloc: a static device array
+ * of W4_NOALLOC_SCRATCH_BYTES in every GPU context that loads the library.
  * Asynchrony: every call enqueues work on the caller's stream and returns without
  * synchronizing.  On a validation failure a call returns before launching anything
  * and leaves every output untouched.
  * Thread safety: calls may be made from any host thread; the only process-wide
- * state is a cache of per-device attributes and the test hooks at the end.
+ * state is a cache of per-device attributes (including the device address of that
+ * scratch array) and the test hooks at the end.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -46,7 +49,9 @@ typedef enum {
     W4_ERR_UNSUPPORTED = 2,   /* valid but not implemented: group size other than 128 */
     W4_ERR_MISALIGNED = 3,    /* a pointer violates the alignment stated below */
     W4_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
-    W4_ERR_TIMEOUT = 5        /* a kernel gave up a bounded wait (see w4_check_device_error) */
+    W4_ERR_TIMEOUT = 5,       /* a kernel gave up a bounded wait (see w4_check_device_error) */
+    W4_ERR_SCRATCH_LIMIT = 6  /* w4_matmul_w4a8_noalloc: the shape needs more scratch than
+                                 W4_NOALLOC_SCRATCH_BYTES */
 } w4_status;
 
 /* Element types: of W for w4_quantize_pack / w4_quantize_pack_sym (F16, F32), of the
@@ -142,6 +147,39 @@ W4_API int w4_quantize_pack_percentile(const void *W, int w_dtype, int64_t N, in
 W4_API int w4_quantize_pack_mse(const void *W, int w_dtype, int64_t N, int64_t K, int group,
                                 int candidates, uint8_t *qweight, void *scales, uint8_t *zeros,
                                 cudaStream_t stream);
+
+/*
+ * w4_matmul_w4a8_noalloc -- w4_matmul_w4a8 for callers that cannot allocate device
+ * memory: the same computation, arguments and results, but the scratch that
+ * w4_matmul_w4a8 takes from the caller (on shapes outside the decode path) comes from a
+ * fixed array inside the library, W4_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU that
+ * loads the library, held until the process exits.  The sources have no counterpart of
+ * this call; it exists for the library's users.
+ *
+ * Who needs it: callers that cannot or must not allocate device memory at the point of
+ * the call: plugins and extensions whose host framework owns all device memory through
+ * its own pool and gives them no way into it; real-time inference loops that must not
+ * allocate after start-up, because an allocation can synchronize the device and stall
+ * the loop; code paths with no way to recover from an allocation failure.
+ *
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * Limit: shapes whose scratch (w4_matmul_w4a8_workspace_size(M, K), i.e. M * K * 2
+ *   bytes off the decode path) exceeds W4_NOALLOC_SCRATCH_BYTES return
+ *   W4_ERR_SCRATCH_LIMIT before anything is launched; decode shapes need none.
+ * First call on a device: looks up the array's device address (cudaGetSymbolAddress,
+ *   once per device, with that device current) and caches it.  Make that first call on
+ *   each device before any stream capture begins.
+ * Sharing: every call on a device uses the same array, and it keeps what the last call
+ *   left there.  Nothing in it needs to start at zero: each call writes the part it
+ *   reads (the widened activations) before reading it.  Calls whose work overlaps on the
+ *   GPU (on different streams, or from different host threads without ordering) race on
+ *   the array and corrupt each other's results; order them on one stream or with events.
+ * Errors: as w4_matmul_w4a8, plus W4_ERR_SCRATCH_LIMIT.
+ */
+#define W4_NOALLOC_SCRATCH_BYTES (16u << 20)
+W4_API int w4_matmul_w4a8_noalloc(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N, int64_t K,
+                                  int group, const uint8_t *qweight, const void *scales,
+                                  const uint8_t *zeros, void *Y, cudaStream_t stream);
 
 /*
  * w4_gptq_quantize -- GPTQ: quantize W[N,K] into the layout of w4_quantize_pack (4-bit

@@ -19,6 +19,8 @@ W4_ERR_UNSUPPORTED = 2
 W4_ERR_MISALIGNED = 3
 W4_ERR_CUDA = 4
 W4_ERR_TIMEOUT = 5
+W4_ERR_SCRATCH_LIMIT = 6
+W4_NOALLOC_SCRATCH_BYTES = 16 << 20
 W4_DTYPE_F16 = 0
 W4_DTYPE_F32 = 1
 W4_DTYPE_BF16 = 2
@@ -27,7 +29,8 @@ GROUP_SIZE = 128
 # Symbols declared in include/w4a16.h (checked by the host-side tests).
 EXPORTED = ("w4_quantize_pack", "w4_quantize_pack_sym", "w4_quantize_pack_percentile",
             "w4_quantize_pack_mse", "w4_dequantize", "w4_matmul", "w4_quantize_act_int8",
-            "w4_matmul_w4a8", "w4_matmul_w4a8_workspace_size", "w4_gptq_quantize",
+            "w4_matmul_w4a8", "w4_matmul_w4a8_workspace_size", "w4_matmul_w4a8_noalloc",
+            "w4_gptq_quantize",
             "w4_status_string", "w4_check_device_error", "w4_set_wait_timeout_ns",
             "w4_debug_inject_stall")
 
@@ -70,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_matmul_w4a8_workspace_size.restype = ctypes.c_size_t
     lib.w4_matmul_w4a8.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.w4_matmul_w4a8.restype = ctypes.c_int
+    lib.w4_matmul_w4a8_noalloc.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp]
+    lib.w4_matmul_w4a8_noalloc.restype = ctypes.c_int
     lib.w4_gptq_quantize.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp]
     lib.w4_gptq_quantize.restype = ctypes.c_int
     lib.w4_status_string.argtypes = [ctypes.c_int]
@@ -137,6 +142,13 @@ def w4_matmul_w4a8(aq_ptr: int, ascale_ptr: int, M: int, N: int, K: int, group: 
                    scales_ptr: int, zeros_ptr: int, Y_ptr: int, ws_ptr: int, ws_bytes: int, stream: int) -> int:
     return load_library().w4_matmul_w4a8(aq_ptr, ascale_ptr, M, N, K, group, qweight_ptr, scales_ptr, zeros_ptr,
                                          Y_ptr, ws_ptr, ws_bytes, stream)
+
+
+def w4_matmul_w4a8_noalloc(aq_ptr: int, ascale_ptr: int, M: int, N: int, K: int, group: int, qweight_ptr: int,
+                           scales_ptr: int, zeros_ptr: int, Y_ptr: int, stream: int) -> int:
+    """w4_matmul_w4a8 without a caller workspace: scratch from the library's fixed array."""
+    return load_library().w4_matmul_w4a8_noalloc(aq_ptr, ascale_ptr, M, N, K, group, qweight_ptr, scales_ptr,
+                                                 zeros_ptr, Y_ptr, stream)
 
 
 def w4_gptq_quantize(W_ptr: int, w_dtype: int, N: int, K: int, group: int, U_ptr: int, qweight_ptr: int,

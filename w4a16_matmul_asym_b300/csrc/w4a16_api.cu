@@ -21,6 +21,12 @@
 #include "quantize_calib.cuh"
 #include "quantize_pack.cuh"
 
+// Scratch of w4_matmul_w4a8_noalloc: a fixed device array, part of the library's image
+// on every GPU that loads it (held until the process exits), so that entry point never
+// allocates.  Host code must not pass its name to a kernel: the name is a host-side
+// stand-in; the device address comes from cudaGetSymbolAddress (noalloc_scratch below).
+static __device__ __align__(256) uint8_t g_w4a8_noalloc_scratch[W4_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
@@ -49,6 +55,25 @@ int current_sm_count(int *sm_count) {
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Device address of the no-allocation scratch array on the current device, looked up
+// once per device (with that device current) and cached.
+struct ScratchAddr {
+    std::once_flag once;
+    void *ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4_ERR_CUDA;
+    ScratchAddr &sa = g_scratch_addr[dev];
+    std::call_once(sa.once, [&]() { sa.err = cudaGetSymbolAddress(&sa.ptr, g_w4a8_noalloc_scratch); });
+    if (sa.err != cudaSuccess || sa.ptr == nullptr) return W4_ERR_CUDA;
+    *out = sa.ptr;
+    return W4_OK;
+}
 
 w4::WaitParams wait_params() {
     w4::WaitParams w;
@@ -443,6 +468,8 @@ const char *w4_status_string(int status) {
         case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED: pointer alignment violated";
         case W4_ERR_CUDA: return "W4_ERR_CUDA: CUDA call or kernel launch failed";
         case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        case W4_ERR_SCRATCH_LIMIT:
+            return "W4_ERR_SCRATCH_LIMIT: the call needs more scratch than the library's fixed array holds";
         default: return "unknown w4a16 status";
     }
 }
@@ -595,6 +622,21 @@ int w4_matmul_w4a8(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N
                         abf, n8))
         return rc;
     return w4::launch_gemm_tcgen05(abf, M, N, K, qweight, s, zeros, y, stream, sms, wait_params(), a_scale);
+}
+
+int w4_matmul_w4a8_noalloc(const int8_t *a_q, const float *a_scale, int64_t M, int64_t N, int64_t K, int group,
+                           const uint8_t *qweight, const void *scales, const uint8_t *zeros, void *Y,
+                           cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || group <= 0) return W4_ERR_INVALID_ARG;
+    if (group != W4_GROUP_SIZE) return W4_ERR_UNSUPPORTED;
+    if (K % group != 0) return W4_ERR_INVALID_ARG;
+    const size_t need = w4_matmul_w4a8_workspace_size(M, K);
+    if (need > W4_NOALLOC_SCRATCH_BYTES) return W4_ERR_SCRATCH_LIMIT;   // before anything is launched
+    void *scratch = nullptr;
+    if (need > 0 && M > 0 && N > 0) {
+        if (int rc = noalloc_scratch(&scratch)) return rc;
+    }
+    return w4_matmul_w4a8(a_q, a_scale, M, N, K, group, qweight, scales, zeros, Y, scratch, need, stream);
 }
 
 int w4_gptq_quantize(const void *W, int w_dtype, int64_t N, int64_t K, int group, const float *U,
