@@ -19,9 +19,12 @@
 //   warp 0        TMA producer of the activation tiles [MT x 64] bf16
 //   warp 1        allocates all 512 TMEM columns and runs the MMA loop; one elected
 //                 lane issues the MMAs and their commits
-//   warp 2        TMA producer of the packed W tiles [128 x 32 B], on a ring of its own
-//                 so that dequantization runs ahead of the MMAs, bounded only by the
-//                 TMEM A stages, and its latency stays off the MMAs' path
+//   warp 2        TMA producer of the packed W tiles, one quantization group (two
+//                 k-blocks, [128 x 64 B], 64-byte swizzle) per copy, on a ring of its
+//                 own so that dequantization runs ahead of the MMAs, bounded only by the
+//                 TMEM A stages, and its latency stays off the MMAs' path.  A whole group
+//                 per copy halves the copies' row requests; the swizzle spreads the
+//                 dequantize threads' 16-byte reads (row pitch 64 B) over all banks
 //   warps 4-11    epilogue: two warps per TMEM lane quarter, each draining half of the
 //                 accumulator columns, 32 at a time, to bf16.  The accumulator is handed
 //                 back to the MMA warp as soon as the last column is in registers; the
@@ -29,11 +32,11 @@
 //                 tensor store per warp and tile, which runs under the next tile's MMAs
 //                 (direct 2-byte stores instead when Y's rows are not 16-byte aligned)
 //   warps 12-19   dequantize: two warps per lane quarter; thread = one row of the W
-//                 tile, 32 of its 64 k of each k-block, one quantization group (two
-//                 k-blocks) per iteration -> tcgen05.st into two TMEM A stages
+//                 tile, 32 of its 64 k of each k-block, one quantization group (one W
+//                 stage, two k-blocks) per iteration -> tcgen05.st into two TMEM A stages
 // TMEM: columns [0, 256) accumulators (two of 128 when MT <= 128, one of 256 otherwise),
 // columns [256, 512) eight A-operand stages of 32 columns (64 bf16 per lane).
-// Shared memory: 4 activation stages (32 KB), 8 packed-W stages (4 KB), then the
+// Shared memory: 4 activation stages (32 KB), 4 packed-W stages (8 KB), then the
 // epilogue's 8 x 8 KB store-staging blocks.
 // Every wait is bounded (see common.cuh); on a timeout the CTA drains its copies and
 // MMAs, frees TMEM and exits, leaving W4_ERR_TIMEOUT in the device error word.
@@ -53,10 +56,10 @@ constexpr int BW = 128;                       // W rows per tile (MMA M, TMEM la
 constexpr int BK = 64;                        // k per stage
 constexpr int MT_MAX = 256;                   // activation rows per tile (MMA N), max
 constexpr int SA = 4;                         // activation smem stages
-constexpr int SW = 8;                         // packed-W smem stages
+constexpr int SW = 4;                         // packed-W smem stages (one quantization group each)
 constexpr int ST = 8;                         // TMEM A-operand stages
 constexpr int ACT_STAGE_MAX = MT_MAX * BK * 2;  // 32 KB
-constexpr int BQ_STAGE = BW * BK / 2;         // 4 KB
+constexpr int BQ_STAGE = BW * BK;             // 8 KB: 128 rows x 64 B (two k-blocks)
 constexpr int NUM_THREADS = 640;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
@@ -66,7 +69,7 @@ constexpr uint32_t BAR_EPI = 1;               // named barrier of the epilogue w
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;            // accumulator region
 constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
-static_assert(SW % 2 == 0 && ST % 2 == 0, "dequantize warps take W and A stages in pairs");
+static_assert(ST % 2 == 0, "dequantize warps take TMEM A stages in pairs");
 
 constexpr int Y_WARP_BYTES = (MT_MAX / 2) * 32 * 2;  // one epilogue warp's [m][32 n] bf16 block
 
@@ -238,8 +241,8 @@ __device__ __forceinline__ uint32_t bf16_bits(float f) {
 
 // One TMA producer thread: for each k-block of this CTA's tiles in order, waits for a
 // free stage of its ring and copies one box into it (activations: [mt x 64] at
-// (k, m); packed W: [128 x 32 B] at (k / 2, n)).  On an abort it waits for every copy
-// it issued to land before returning.
+// (k, m), one per k-block; packed W: [128 x 64 B] at (k / 2, n), one per pair of
+// k-blocks).  On an abort it waits for every copy it issued to land before returning.
 template <int S, bool kW>
 __device__ __forceinline__ void produce(const CUtensorMap *map, uint8_t *ring, uint32_t stage_bytes,
                                         uint32_t tx_bytes, uint64_t *full, uint64_t *empty,
@@ -253,7 +256,7 @@ __device__ __forceinline__ void produce(const CUtensorMap *map, uint8_t *ring, u
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const int mi = tile % m_tiles, ni = tile / m_tiles;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = 0; kb < KB; kb += (kW ? 2 : 1)) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, tmo)) {
                 ok = false;
                 break;
@@ -564,19 +567,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t zb = bf16_bits(128.0f + static_cast<float>(z_cur));
                 const uint32_t s2 = sb | (sb << 16);
                 const uint32_t zz2 = zb | (zb << 16);
-                if (!warp_wait(&w_full[ws], wphase, abort_flag, tmo) ||
-                    !warp_wait(&w_full[ws + 1], wphase, abort_flag, tmo)) {
+                if (!warp_wait(&w_full[ws], wphase, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *wsrc = smem + OFF_W + ws * BQ_STAGE + r * 32 + half * 16;
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(wsrc);
-                const uint4 w1 = *reinterpret_cast<const uint4 *>(wsrc + BQ_STAGE);
+                const uint8_t *wrow = smem + OFF_W + ws * BQ_STAGE + r * 64;
+                const int swz = (r >> 1) & 3;
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(wrow + 16 * (half ^ swz));
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(wrow + 16 * ((2 + half) ^ swz));
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&w_empty[ws]);
-                    mbar_arrive(&w_empty[ws + 1]);
-                }
+                if (lane == 0) mbar_arrive(&w_empty[ws]);
                 if (!warp_wait(&a_empty[as], aphase ^ 1u, abort_flag, tmo) ||
                     !warp_wait(&a_empty[as + 1], aphase ^ 1u, abort_flag, tmo)) {
                     ok = false;
@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive(&a_full[as]);
                     mbar_arrive(&a_full[as + 1]);
                 }
-                if ((ws += 2) == SW) {
+                if (++ws == SW) {
                     ws = 0;
                     wphase ^= 1u;
                 }
@@ -663,8 +663,8 @@ inline int launch_gemm_tcgen05(const __nv_bfloat16 *A, int64_t M, int64_t N, int
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, BK, mt,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return W4_ERR_CUDA;
-    if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, K / 2, N, K / 2, BK / 2, BW,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, K / 2, N, K / 2, BK, BW,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
         return W4_ERR_CUDA;
     // Y by tensor stores when its base and row pitch are 16-byte aligned: box of 32 n
     // (64 bytes) by mt / 2 rows of m, one per epilogue warp and tile.

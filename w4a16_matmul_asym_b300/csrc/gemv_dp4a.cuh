@@ -93,7 +93,7 @@ struct Layout {
         off_red = off_ring + S * stage_b;
         off_dig = off_red + up128(RS * R * (32 * WR + 1) * 4);
         off_sv = off_dig + up128(pieces * PAD * 4);
-        off_csc = off_sv + up128(pieces * 4);
+        off_csc = off_sv + up128((K / 16) * 4);   // one digit sum per 16-level segment
         off_res = off_csc + up128(ng * 4);         // activations, then their residuals
         off_cmask = off_res + up128(K * 2);
         off_bar = off_cmask + up128((K / 32) * 4);
@@ -162,7 +162,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
     uint8_t *ring = smem + L.off_ring;
     float *red = reinterpret_cast<float *>(smem + L.off_red);
     uint32_t *dig = reinterpret_cast<uint32_t *>(smem + L.off_dig);
-    int *svs = reinterpret_cast<int *>(smem + L.off_sv);
+    int *svs = reinterpret_cast<int *>(smem + L.off_sv);          // [K / 16] digit sums
+    // Per-segment exponent maxima, only during the conversion: they share the reduction
+    // ring (RS * R * (32 WR + 1) floats >= 8 KB >= K / 16 words), untouched until then.
+    uint32_t *lmx = reinterpret_cast<uint32_t *>(smem + L.off_red);
+    unsigned short *cmask16 = reinterpret_cast<unsigned short *>(smem + L.off_cmask);
     float *cscs = reinterpret_cast<float *>(smem + L.off_csc);
     unsigned short *res = reinterpret_cast<unsigned short *>(smem + L.off_res);
     uint32_t *cmask = reinterpret_cast<uint32_t *>(smem + L.off_cmask);
@@ -247,18 +251,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
         __syncwarp();
     } else {
         // ---------------- activations -> digits (all non-producer warps) ----------------
-        // One thread per 16 levels (two packed words); the 8 threads of a group are
-        // consecutive lanes of one warp, so the group maximum and the piece sums take
-        // three xor shuffles and everything else stays in the thread.
+        // One thread per 16-level segment (two packed words).  No warp shuffles: the
+        // group maximum goes through shared memory (each segment's maximum, a barrier,
+        // then the eight of its group), and each segment stores its own digit sum and
+        // left-out flags, which the consumers combine per lane.
         const int nconv = (CW + 1) * 32;
         const int cw_id = warp < CW ? warp : CW;   // epilogue warp takes the last slot
         const bool have_a = warp_wait_full_bounded(a_bar, 0, abort_flag, tmo);
-        for (int base = cw_id * 32; I8 && have_a && base < K / 16; base += nconv) {
+        for (int sg = cw_id * 32 + lane; I8 && have_a && sg < K / 16; sg += nconv) {
             // int8 activations: the digit words are byte permutes (levels 0 2 4 6 and
             // 1 3 5 7 of each packed word), one signed digit, no residuals.
-            const int sg = base + lane;
-            const bool act = sg < K / 16;
-            const uint4 x = act ? reinterpret_cast<const uint4 *>(res)[sg] : make_uint4(0, 0, 0, 0);
+            const uint4 x = reinterpret_cast<const uint4 *>(res)[sg];
             uint32_t dw[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}};
             dw[0][0] = byte_perm(x.x, x.y, 0x6420u);
             dw[0][3] = byte_perm(x.x, x.y, 0x7531u);
@@ -271,86 +274,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
             const int g = sg >> 3;
             const int piece = g * H + (sg & 7) / (8 / H);
             const int wi = ((sg & 7) % (8 / H)) * 2;
-            const int l = piece & 31;
             const int cpos = wi >> 2;
-            const int slot = (cpos - lane_rot<H>(l)) & (NCH - 1);
-#pragma unroll
-            for (int o = 1; o < 8 / H; o <<= 1) vsum += __shfl_xor_sync(0xffffffffu, vsum, o);
-            if (act) {
-                uint4 *dst = reinterpret_cast<uint4 *>(dig + piece * PAD + (slot * 4 + (wi & 3)) * 6);
-                dst[0] = make_uint4(dw[0][0], dw[0][1], dw[0][2], dw[0][3]);
-                dst[1] = make_uint4(dw[0][4], dw[0][5], dw[1][0], dw[1][1]);
-                dst[2] = make_uint4(dw[1][2], dw[1][3], dw[1][4], dw[1][5]);
-                if ((sg & 1) == 0) cmask[sg >> 1] = 0u;
-                if ((sg & 7) % (8 / H) == 0) svs[piece] = vsum;
-                if ((sg & 7) == 0) cscs[g] = 1.0f;
-            }
+            const int slot = (cpos - lane_rot<H>(piece & 31)) & (NCH - 1);
+            uint4 *dst = reinterpret_cast<uint4 *>(dig + piece * PAD + (slot * 4 + (wi & 3)) * 6);
+            dst[0] = make_uint4(dw[0][0], dw[0][1], dw[0][2], dw[0][3]);
+            dst[1] = make_uint4(dw[0][4], dw[0][5], dw[1][0], dw[1][1]);
+            dst[2] = make_uint4(dw[1][2], dw[1][3], dw[1][4], dw[1][5]);
+            cmask16[sg] = 0;
+            svs[sg] = vsum;
+            if ((sg & 7) == 0) cscs[g] = 1.0f;
         }
-        for (int base = cw_id * 32; !I8 && have_a && base < K / 16; base += nconv) {
-            const int sg = base + lane;            // 16-level segment; K / 16 is a multiple of 8
-            const bool act = sg < K / 16;
-            uint32_t w[8];                         // 16 bf16, two per word, natural order
-            {
+        if constexpr (!I8) {
+            // Pass 1: each segment's maximum of the exponent|mantissa bits (infinities
+            // and NaNs included: such a group sends all its finite elements to the
+            // residual path).
+            for (int sg = cw_id * 32 + lane; have_a && sg < K / 16; sg += nconv) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(res) + sg * 2;
-                const uint4 x0 = act ? src[0] : make_uint4(0, 0, 0, 0);
-                const uint4 x1 = act ? src[1] : make_uint4(0, 0, 0, 0);
-                w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
-                w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
+                const uint4 x0 = src[0], x1 = src[1];
+                uint32_t mx = vmax_u16x2(x0.x & 0x7FFF7FFFu, x0.y & 0x7FFF7FFFu);
+                mx = vmax_u16x2(mx, x0.z & 0x7FFF7FFFu);
+                mx = vmax_u16x2(mx, x0.w & 0x7FFF7FFFu);
+                mx = vmax_u16x2(mx, x1.x & 0x7FFF7FFFu);
+                mx = vmax_u16x2(mx, x1.y & 0x7FFF7FFFu);
+                mx = vmax_u16x2(mx, x1.z & 0x7FFF7FFFu);
+                mx = vmax_u16x2(mx, x1.w & 0x7FFF7FFFu);
+                lmx[sg] = max(mx & 0xFFFFu, mx >> 16);
             }
-            // Group maximum of the exponent|mantissa bits (infinities and NaNs included:
-            // such a group sends all its finite elements to the residual path).
-            uint32_t mx = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx = vmax_u16x2(mx, w[i] & 0x7FFF7FFFu);
-            mx = max(mx & 0xFFFFu, mx >> 16);
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const int emax = max(static_cast<int>(mx >> 7), 1);  // exponent field, >= 1
-            // v = a * 2^c, c = 146 - emax, |v| < 2^20; exact iff |a| >= 2^(emax - 139).
-            const int c = 146 - emax;
-            const float c1 = pow2f(min(c, 127)), c2 = pow2f(max(c - 127, 0));
-            const float thr = pow2f(emax - 139);
-            int v[16];
-            uint32_t flag = 0;
-            int vsum = 0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float a = __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
-                const float tt = __fmaf_rn(__fmul_rn(a, c1), c2, 12582912.0f);  // 1.5 * 2^23: round to integer
-                const int vi = __float_as_int(tt) - 0x4B400000;
-                const float m = fabsf(a);
-                const bool left_out = !(m <= 3.402823466e38f) || (m != 0.0f && m < thr);  // inf / NaN, or too small
-                v[i] = left_out ? 0 : vi;
-                vsum += v[i];
-                flag |= static_cast<uint32_t>(left_out) << i;
-            }
-            // Digit words of each packed word: even levels (0, 2, 4, 6), odd levels
-            // (1, 3, 5, 7); byte j of digit word d is byte d of v of the j-th level.
-            uint32_t dw[2][6];
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-                for (int par = 0; par < 2; ++par) {
-                    const uint32_t va = static_cast<uint32_t>(v[8 * q + par]), vb = static_cast<uint32_t>(v[8 * q + 2 + par]);
-                    const uint32_t vc = static_cast<uint32_t>(v[8 * q + 4 + par]), vd = static_cast<uint32_t>(v[8 * q + 6 + par]);
-                    const uint32_t lo_ab = byte_perm(va, vb, 0x5140u), lo_cd = byte_perm(vc, vd, 0x5140u);
-                    const uint32_t hi_ab = byte_perm(va, vb, 0x0062u), hi_cd = byte_perm(vc, vd, 0x0062u);
-                    dw[q][3 * par + 0] = byte_perm(lo_ab, lo_cd, 0x5410u);
-                    dw[q][3 * par + 1] = byte_perm(lo_ab, lo_cd, 0x7632u);
-                    dw[q][3 * par + 2] = byte_perm(hi_ab, hi_cd, 0x5410u);
+            asm volatile("bar.sync 2, %0;" ::"r"((CW + 1) * 32) : "memory");
+            // Pass 2: the digits.
+            for (int sg = cw_id * 32 + lane; have_a && sg < K / 16; sg += nconv) {
+                uint32_t w[8];                     // 16 bf16, two per word, natural order
+                {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(res) + sg * 2;
+                    const uint4 x0 = src[0], x1 = src[1];
+                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+                    w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
                 }
-            // Piece (lane slot) of this segment and its place in the lane's rotated order.
-            const int g = sg >> 3;                   // 8 segments per group
-            const int piece = g * H + (sg & 7) / (8 / H);
-            const int wi = ((sg & 7) % (8 / H)) * 2;  // first packed word within the piece
-            const int l = piece & 31;
-            const int cpos = wi >> 2;                // chunk within the piece
-            const int slot = (cpos - lane_rot<H>(l)) & (NCH - 1);
-            // Per piece: sum of v (the 8 / H segments of a piece are consecutive lanes).
+                const int g = sg >> 3;             // 8 segments per group
+                uint32_t mx;
+                {
+                    const uint4 m0 = reinterpret_cast<const uint4 *>(lmx)[2 * g];
+                    const uint4 m1 = reinterpret_cast<const uint4 *>(lmx)[2 * g + 1];
+                    mx = max(max(max(m0.x, m0.y), max(m0.z, m0.w)), max(max(m1.x, m1.y), max(m1.z, m1.w)));
+                }
+                const int emax = max(static_cast<int>(mx >> 7), 1);  // exponent field, >= 1
+                // v = a * 2^c, c = 146 - emax, |v| < 2^20; exact iff |a| >= 2^(emax - 139).
+                const int c = 146 - emax;
+                const float c1 = pow2f(min(c, 127)), c2 = pow2f(max(c - 127, 0));
+                const float thr = pow2f(emax - 139);
+                int v[16];
+                uint32_t flag = 0;
+                int vsum = 0;
 #pragma unroll
-            for (int o = 1; o < 8 / H; o <<= 1) vsum += __shfl_xor_sync(0xffffffffu, vsum, o);
-            const uint32_t fpair = __shfl_xor_sync(0xffffffffu, flag, 1);
-            if (act) {
+                for (int i = 0; i < 16; ++i) {
+                    const float a = __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
+                    const float tt = __fmaf_rn(__fmul_rn(a, c1), c2, 12582912.0f);  // 1.5 * 2^23: round to integer
+                    const int vi = __float_as_int(tt) - 0x4B400000;
+                    const float m = fabsf(a);
+                    const bool left_out = !(m <= 3.402823466e38f) || (m != 0.0f && m < thr);  // inf / NaN, or too small
+                    v[i] = left_out ? 0 : vi;
+                    vsum += v[i];
+                    flag |= static_cast<uint32_t>(left_out) << i;
+                }
+                // Digit words of each packed word: even levels (0, 2, 4, 6), odd levels
+                // (1, 3, 5, 7); byte j of digit word d is byte d of v of the j-th level.
+                uint32_t dw[2][6];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int par = 0; par < 2; ++par) {
+                        const uint32_t va = static_cast<uint32_t>(v[8 * q + par]), vb = static_cast<uint32_t>(v[8 * q + 2 + par]);
+                        const uint32_t vc = static_cast<uint32_t>(v[8 * q + 4 + par]), vd = static_cast<uint32_t>(v[8 * q + 6 + par]);
+                        const uint32_t lo_ab = byte_perm(va, vb, 0x5140u), lo_cd = byte_perm(vc, vd, 0x5140u);
+                        const uint32_t hi_ab = byte_perm(va, vb, 0x0062u), hi_cd = byte_perm(vc, vd, 0x0062u);
+                        dw[q][3 * par + 0] = byte_perm(lo_ab, lo_cd, 0x5410u);
+                        dw[q][3 * par + 1] = byte_perm(lo_ab, lo_cd, 0x7632u);
+                        dw[q][3 * par + 2] = byte_perm(hi_ab, hi_cd, 0x5410u);
+                    }
+                // Piece (lane slot) of this segment and its place in the lane's rotated order.
+                const int piece = g * H + (sg & 7) / (8 / H);
+                const int wi = ((sg & 7) % (8 / H)) * 2;  // first packed word within the piece
+                const int cpos = wi >> 2;                // chunk within the piece
+                const int slot = (cpos - lane_rot<H>(piece & 31)) & (NCH - 1);
                 uint4 *dst = reinterpret_cast<uint4 *>(dig + piece * PAD + (slot * 4 + (wi & 3)) * 6);
                 dst[0] = make_uint4(dw[0][0], dw[0][1], dw[0][2], dw[0][3]);
                 dst[1] = make_uint4(dw[0][4], dw[0][5], dw[1][0], dw[1][1]);
@@ -366,16 +371,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
                 uint4 *rdst = reinterpret_cast<uint4 *>(res) + sg * 2;
                 rdst[0] = make_uint4(rw[0], rw[1], rw[2], rw[3]);
                 rdst[1] = make_uint4(rw[4], rw[5], rw[6], rw[7]);
-                if ((sg & 1) == 0) cmask[sg >> 1] = flag | (fpair << 16);
-                if ((sg & 7) % (8 / H) == 0) svs[piece] = vsum;
+                cmask16[sg] = static_cast<unsigned short>(flag);
+                svs[sg] = vsum;
                 if ((sg & 7) == 0) cscs[g] = pow2f(emax - 146);
             }
         }
     }
     if (warp != PROD_WARP) {
-        // Lane slots beyond the row's pieces contribute nothing.
-        for (int i = threadIdx.x; i < 32 * WR; i += PROD_WARP * 32)
-            if (i >= ng * H) svs[i] = 0;
         // Named barrier of the non-producer warps: the producer is already streaming.
         asm volatile("bar.sync 1, %0;" ::"r"((CW + 1) * 32) : "memory");
     }
@@ -431,7 +433,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
         }
         const int wlist = __reduce_max_sync(0xffffffffu, cnt > 4 ? 0 : cnt);  // warp-uniform
         const bool wslow = __any_sync(0xffffffffu, cnt > 4);
-        const int sv = active ? svs[piece] : 0;
+        int sv = 0;                                // sum of v over the lane's piece
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < 8 / H; ++i) sv += svs[piece * (8 / H) + i];
+        }
         const float csc = active ? cscs[g] : 0.0f;
         const int wbyte = g * 64 + hh * 32;
         bool ok = true;

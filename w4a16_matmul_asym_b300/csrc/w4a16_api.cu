@@ -175,6 +175,8 @@ int launch_gemv_dp4a(const void *A, bool i8, const float *row_scale, int64_t N, 
     int WR = 1;
     while (WR <= gd::CW && (32 * WR < H * ng || gd::CW % WR != 0)) ++WR;
     if (WR > gd::CW) return W4_ERR_UNSUPPORTED;
+    // The conversion's per-segment maxima (K / 16 words) borrow the reduction ring.
+    if (static_cast<int64_t>(gd::RS) * (gd::CW / WR) * gd::RB * (32 * WR + 1) < k / 16) return W4_ERR_UNSUPPORTED;
     int stages = 0, smem = 0;
     for (int s = gd::MAX_STAGES; s >= 2; --s) {
         const int total = H == 1 ? gd::Layout<1>(k, WR, s).total : gd::Layout<2>(k, WR, s).total;
