@@ -191,14 +191,10 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
     return true;
 }
 
-// Lane 0 waits, the result is broadcast, so the warp leaves the wait converged.
+// The whole warp waits (common.cuh: every lane polls, a vote decides).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned long long timeout_ns) {
-    int ok = 1;
-    if (lane_id() == 0) ok = mbar_wait(bar, parity, abort_flag, timeout_ns) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();  // orders the other lanes' accesses after lane 0's acquire
-    return ok != 0;
+    return warp_mbar_wait(bar, parity, abort_flag, timeout_ns);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -478,12 +474,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (c0 + 8 * j < cols) tmem_ld_8cols(tbase + c0 + 8 * j, v + 8 * j);
                 tmem_wait_ld();
                 if (p.row_scale != nullptr) {
-                    // Column j of this chunk is activation row m0 + c0 + j: scale it in fp32.
-                    const int mr = m0 + c0 + lane;
-                    const float rs = p.row_scale[mr < p.M ? mr : p.M - 1];
+                    // Column j of this chunk is activation row m0 + c0 + j: scale it in fp32
+                    // (the same address in every lane: one broadcast load per column).
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), __shfl_sync(0xffffffffu, rs, j)));
+                    for (int j = 0; j < 32; ++j) {
+                        const int mr = m0 + c0 + j;
+                        const float rs = __ldg(p.row_scale + (mr < p.M ? mr : p.M - 1));
+                        v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), rs));
+                    }
                 }
                 if (c0 + 32 >= cols) {
                     // This warp's part of the accumulator is in registers: hand it back.

@@ -103,7 +103,10 @@ struct Layout {
     __host__ __device__ int fixed() const { return total - S * stage_b; }
 };
 
-// Lane 0 waits (bounded), the result is broadcast, the warp leaves converged.
+// Lane 0 waits (bounded), the result is broadcast, the warp leaves converged.  (The
+// vote-based warp_mbar_wait of common.cuh measured slower here: this kernel's epilogue
+// warp waits microseconds at a time, and 32 polling lanes compete with the consumers'
+// shared-memory traffic.)
 __device__ __forceinline__ bool warp_wait_full_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                                        unsigned long long tmo) {
     int ok = 1;

@@ -193,16 +193,10 @@ __device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
-// One lane waits (bounded), the warp follows its verdict.
+// The whole warp waits (common.cuh: every lane polls, a vote decides).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned long long tmo, bool polite) {
-    int got = 1;
-    if (lane_id() == 0)
-        got = (polite ? mbar_wait_polite(bar, parity, abort_flag, tmo) : mbar_wait(bar, parity, abort_flag, tmo))
-                  ? 1 : 0;
-    got = __shfl_sync(0xffffffffu, got, 0);
-    __syncwarp();
-    return got != 0;
+    return warp_mbar_wait(bar, parity, abort_flag, tmo, polite);
 }
 
 // ---- producer warp ----------------------------------------------------------------------
@@ -363,8 +357,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---- consumers: stage the activations, permuted: the 16-byte chunk (g, v, m, t)
     // (index ((4 g + v) M + m) 4 + t) holds A[m, 128 g + 32 t + 8 v + (0 4 1 5 2 6 3 7)]
-    // as bf16.  Threads walk the chunks in shared-memory order, so the stores are
-    // conflict-free.
+    // as bf16.  Threads walk A in its natural order, so each warp's loads are contiguous
+    // (coalesced), and scatter the permuted chunks into shared memory.
     const uint32_t a_base = smem_addr(smem);
     {
         const int total = M * (K >> 3);
@@ -376,10 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int c = c0 + u * CW * 32;
                 nat[u] = make_uint4(0, 0, 0, 0);
                 if (c < total) {
-                    const int t = c & 3, rest = c >> 2;
-                    const int m = rest % M, gv = rest / M;
-                    const int g = gv >> 2, v = gv & 3;
-                    const int64_t e = static_cast<int64_t>(m) * K + g * 128 + t * 32 + v * 8;
+                    const int64_t e = static_cast<int64_t>(c) * 8;
                     if constexpr (I8) {
                         const uint2 q = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(p.A) + e));
                         nat[u] = make_uint4(q.x, q.y, 0, 0);
@@ -395,7 +386,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint4 v;
                     if constexpr (I8) v = pair_permute_i8(make_uint2(nat[u].x, nat[u].y));
                     else v = pair_permute(nat[u]);
-                    sts128(a_base + (static_cast<uint32_t>(c) << 4), v);
+                    const int m = c / (K >> 3), kc = c - m * (K >> 3);
+                    const int g = kc >> 4, t = (kc >> 2) & 3, vv = kc & 3;
+                    const int d = (((4 * g + vv) * M + m) << 2) + t;
+                    sts128(a_base + (static_cast<uint32_t>(d) << 4), v);
                 }
             }
         }
