@@ -439,6 +439,18 @@ def test_matmul_gemm_many_tiles_full(env, M, N, K):
     assert_matmul_ok(env, A, q, s, z)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 19200, 384), (300, 19072, 1024), (768, 6400, 256)])
+def test_matmul_gemm_partial_last_wave_full(env, M, N, K):
+    """Tile counts (150, 298, 150 on 148 SMs) that leave a last wave of two tiles, so a
+    few CTAs run one tile more than the rest (the persistent loop's end with uneven
+    work), at K = 384, 1024 and 256.  Every output compared."""
+    import synth
+    _, _, orc = env
+    W, A = synth.make_random(N, K, M, seed=M + 7 * N + K)
+    q, s, z = orc.quantize_pack(W)
+    assert_matmul_ok(env, A, q, s, z)
+
+
 def test_matmul_prefill_workload_sampled(env):
     """Full-size prefill workload (M=2048, N=14336, K=4096) in the launch configuration
     the benchmark times; checked on 6000 sampled outputs plus one full output row and

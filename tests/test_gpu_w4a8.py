@@ -95,10 +95,11 @@ def test_w4a8_decode_path(env, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 100, 1152), (17, 257, 2048), (64, 1000, 1024), (300, 777, 640),
-                                   (16, 64, 16384)])
+                                   (16, 64, 16384), (256, 19200, 384)])
 def test_w4a8_gemm_path(env, M, N, K):
     """Shapes the decode kernel does not take: a_q widened into the workspace, then the
-    tcgen05 GEMM with the per-row scale in its epilogue."""
+    tcgen05 GEMM with the per-row scale in its epilogue (256 x 19200: more tiles than
+    SMs, with a partial last wave)."""
     import synth
     torch, w4, orc = env
     assert w4.w4_matmul_w4a8_workspace_size(M, K) >= M * K * 2
