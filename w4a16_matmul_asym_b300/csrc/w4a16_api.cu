@@ -572,11 +572,14 @@ int w4_quantize_act_int8(const void *A, int64_t M, int64_t K, int8_t *a_q, float
     int sms = 0;
     if (int rc = current_sm_count(&sms)) return rc;
     namespace aq = w4::actq;
-    int64_t blocks = (M + aq::WARPS - 1) / aq::WARPS;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (M <= 2 * static_cast<int64_t>(sms))       // few rows: 256 threads on each
+        return launch(aq::act_quant_int8_kernel, dim3(static_cast<unsigned>(M)), dim3(aq::NUM_THREADS), 0, stream,
+                      static_cast<const __nv_bfloat16 *>(A), M, K, a_q, a_scale);
+    int64_t blocks = (M + 7) / 8;                  // many rows: a warp on each
     if (blocks > cap) blocks = cap;
-    return launch(aq::act_quant_int8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(aq::NUM_THREADS), 0, stream,
-                  static_cast<const __nv_bfloat16 *>(A), M, K, a_q, a_scale);
+    return launch(aq::act_quant_int8_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(aq::NUM_THREADS), 0,
+                  stream, static_cast<const __nv_bfloat16 *>(A), M, K, a_q, a_scale);
 }
 
 size_t w4_matmul_w4a8_workspace_size(int64_t M, int64_t K) {
