@@ -68,24 +68,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gptq_kernel(const Params p) {
     const int n0 = blockIdx.x * R;
     const int rows = min(R, p.N - n0);
 
-    // Working rows, widened exactly to fp32 (rows past N are zero and never stored).
-    for (int i = threadIdx.x; i < R * K; i += NUM_THREADS) {
-        const int r = i / K, c = i - r * K;
-        float v = 0.0f;
-        if (r < rows) {
-            const int64_t e = static_cast<int64_t>(n0 + r) * K + c;
-            v = kF32 ? static_cast<const float *>(p.W)[e]
-                     : __half2float(static_cast<const __half *>(p.W)[e]);
+    // Working rows, widened exactly to fp32 (rows past N are zero and never stored);
+    // 8 loads in flight per thread.
+    for (int i0 = threadIdx.x; i0 < R * K; i0 += 8 * NUM_THREADS) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * NUM_THREADS;
+            const int r = i / K, c = i - r * K;
+            v[u] = 0.0f;
+            if (i < R * K && r < rows) {
+                const int64_t e = static_cast<int64_t>(n0 + r) * K + c;
+                v[u] = kF32 ? __ldg(static_cast<const float *>(p.W) + e)
+                            : __half2float(static_cast<const __half *>(p.W)[e]);
+            }
         }
-        w[i] = v;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (i0 + u * NUM_THREADS < R * K) w[i0 + u * NUM_THREADS] = v[u];
     }
 
     for (int b = 0; b < ng; ++b) {
         const int c0 = b * BLK;
         // The block's diagonal part of U: ub[jj][cc] = U[c0 + jj][c0 + cc].
-        for (int i = threadIdx.x; i < BLK * BLK; i += NUM_THREADS) {
-            const int jj = i >> 7, cc = i & (BLK - 1);
-            ub[i] = __ldg(p.U + static_cast<int64_t>(c0 + jj) * K + c0 + cc);
+        // (64 values per thread, 16 loads in flight.)
+#pragma unroll 1
+        for (int i0 = threadIdx.x; i0 < BLK * BLK; i0 += 16 * NUM_THREADS) {
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i = i0 + u * NUM_THREADS;
+                v[u] = __ldg(p.U + static_cast<int64_t>(c0 + (i >> 7)) * K + c0 + (i & (BLK - 1)));
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) ub[i0 + u * NUM_THREADS] = v[u];
         }
         __syncthreads();
 
@@ -108,6 +124,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gptq_kernel(const Params p) {
             const float zp = fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.0f), 15.0f);
             const __half s16 = __float2half_rn(s);
             const float s16f = __half2float(s16);
+            const float rs = __frcp_rn(s);
             if (lane == 0 && r < rows) {
                 p.scales[static_cast<int64_t>(n0 + r) * ng + b] = s16;
                 p.zeros[static_cast<int64_t>(n0 + r) * ng + b] = static_cast<uint8_t>(zp);
@@ -118,7 +135,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gptq_kernel(const Params p) {
                 for (int jl = 0; jl < 32; ++jl) {
                     const int jj = 32 * i + jl;
                     const float x = __shfl_sync(0xffffffffu, wv[i], jl);
-                    const float q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(x, s)), zp), 0.0f), 15.0f);
+                    // rint(x / s) from t = x * fl(1/s): within 2^-15 of a half-integer
+                    // (or NaN) the IEEE quotient decides; beyond |t| > 32 both clip alike.
+                    const float t = __fmul_rn(x, rs);
+                    float rq = rintf(t);
+                    if (!(fabsf(t - rq) <= 0.499969482421875f)) rq = rintf(__fdiv_rn(x, s));
+                    const float q = fminf(fmaxf(__fadd_rn(rq, zp), 0.0f), 15.0f);
                     const float rec = __fmul_rn(__fsub_rn(q, zp), s16f);
                     const float e = __fdiv_rn(__fsub_rn(x, rec), ub[jj * BLK + jj]);
                     if (lane == jl) lev[r * BLK + jj] = static_cast<uint8_t>(q);
@@ -140,20 +162,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gptq_kernel(const Params p) {
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = r < R ? w[r * K + c] : 0.0f;
             const float *ucol = p.U + static_cast<int64_t>(c0) * K + c;
-#pragma unroll 4
-            for (int jj = 0; jj < BLK; ++jj) {
-                const float u = __ldg(ucol + static_cast<int64_t>(jj) * K);
-                const float4 e0 = *reinterpret_cast<const float4 *>(err + jj * 8);
-                const float4 e1 = *reinterpret_cast<const float4 *>(err + jj * 8 + 4);
-                acc[0] = __fmaf_rn(-e0.x, u, acc[0]);
-                acc[1] = __fmaf_rn(-e0.y, u, acc[1]);
-                acc[2] = __fmaf_rn(-e0.z, u, acc[2]);
-                acc[3] = __fmaf_rn(-e0.w, u, acc[3]);
-                if (R > 4) {
-                    acc[4] = __fmaf_rn(-e1.x, u, acc[4]);
-                    acc[5] = __fmaf_rn(-e1.y, u, acc[5]);
-                    acc[6] = __fmaf_rn(-e1.z, u, acc[6]);
-                    acc[7] = __fmaf_rn(-e1.w, u, acc[7]);
+#pragma unroll 1
+            for (int jb = 0; jb < BLK; jb += 32) {
+                float uu[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) uu[k] = __ldg(ucol + static_cast<int64_t>(jb + k) * K);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int jj = jb + k;
+                    const float u = uu[k];
+                    const float4 e0 = *reinterpret_cast<const float4 *>(err + jj * 8);
+                    const float4 e1 = *reinterpret_cast<const float4 *>(err + jj * 8 + 4);
+                    acc[0] = __fmaf_rn(-e0.x, u, acc[0]);
+                    acc[1] = __fmaf_rn(-e0.y, u, acc[1]);
+                    acc[2] = __fmaf_rn(-e0.z, u, acc[2]);
+                    acc[3] = __fmaf_rn(-e0.w, u, acc[3]);
+                    if (R > 4) {
+                        acc[4] = __fmaf_rn(-e1.x, u, acc[4]);
+                        acc[5] = __fmaf_rn(-e1.y, u, acc[5]);
+                        acc[6] = __fmaf_rn(-e1.z, u, acc[6]);
+                        acc[7] = __fmaf_rn(-e1.w, u, acc[7]);
+                    }
                 }
             }
 #pragma unroll
