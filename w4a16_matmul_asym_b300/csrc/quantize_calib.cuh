@@ -187,6 +187,107 @@ __global__ void __launch_bounds__(NUM_THREADS) calib_percentile_kernel(const Par
     }
 }
 
+// Percentiles near either end of the group (lo >= 120, or hi <= 7): one thread per
+// group.  The thread keeps the KT largest (or smallest) magnitudes of its 128 in a
+// sorted register list (each value bubbles through the list: one max and one min per
+// slot), so the two order statistics come without warp exchanges; the levels use
+// t = w * fl(1/s), which gives clamp(rint(w / s), -7, 7) exactly except within 2^-15 of
+// a half-integer (|t - fl(w/s)| <= 8 * 3 * 2^-24 there; beyond |t| > 8 both clamp),
+// where the IEEE quotient is taken.
+template <bool kF32, bool kTop, int KT>
+__global__ void __launch_bounds__(NUM_THREADS) calib_percentile_ends_kernel(const Params p) {
+    const float qf = __fdiv_rn(p.p, 100.0f);
+    const float h = __fmul_rn(qf, 127.0f);
+    const float fl = floorf(h);
+    const int lo = min(max(static_cast<int>(fl), 0), 127);
+    const int hi = min(lo + 1, 127);
+    const float f = __fsub_rn(h, fl);
+    // Positions in the kept list: from the top, a_(127 - r) is entry r; from the bottom, a_r.
+    const int rlo = kTop ? 127 - lo : lo, rhi = kTop ? 127 - hi : hi;
+    constexpr int VPL = kF32 ? 4 : 8;          // values per 16-byte load
+    constexpr int LOADS = 128 / VPL;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * NUM_THREADS + threadIdx.x; g < p.groups;
+         g += static_cast<int64_t>(gridDim.x) * NUM_THREADS) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.W) + g * LOADS;
+        float keep[KT];
+#pragma unroll
+        for (int j = 0; j < KT; ++j) keep[j] = kTop ? -1.0f : __int_as_float(0x7f800000);
+#pragma unroll 4
+        for (int l = 0; l < LOADS; ++l) {
+            const uint4 v = __ldg(src + l);
+            float x[VPL];
+            if constexpr (kF32) {
+                x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+                x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+            } else {
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    x[2 * k] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[k] & 0xFFFFu)));
+                    x[2 * k + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[k] >> 16)));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < VPL; ++e) {
+                float c = fabsf(x[e]);
+                if (!(c == c)) c = kTop ? -1.0f : __int_as_float(0x7f800000);   // NaN: left out
+#pragma unroll
+                for (int j = 0; j < KT; ++j) {
+                    const float a = kTop ? fmaxf(keep[j], c) : fminf(keep[j], c);
+                    c = kTop ? fminf(keep[j], c) : fmaxf(keep[j], c);
+                    keep[j] = a;
+                }
+            }
+        }
+        float alo = keep[0], ahi = keep[0];
+#pragma unroll
+        for (int j = 1; j < KT; ++j) {
+            if (j == rlo) alo = keep[j];
+            if (j == rhi) ahi = keep[j];
+        }
+        const float r = __fadd_rn(alo, __fmul_rn(f, __fsub_rn(ahi, alo)));
+        const float sc = (r == 0.0f) ? 1.0f : __fdiv_rn(r, 7.0f);
+        const float rs = __frcp_rn(sc);
+        // Levels: the group again (L1/L2), 8 levels -> one 32-bit word.
+        uint32_t *dst = reinterpret_cast<uint32_t *>(p.qweight + g * 64);
+        uint32_t prev = 0;
+#pragma unroll 2
+        for (int l = 0; l < LOADS; ++l) {
+            const uint4 v = __ldg(src + l);
+            float x[VPL];
+            if constexpr (kF32) {
+                x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+                x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+            } else {
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    x[2 * k] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[k] & 0xFFFFu)));
+                    x[2 * k + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[k] >> 16)));
+                }
+            }
+            uint32_t word = 0;
+#pragma unroll
+            for (int e = 0; e < VPL; ++e) {
+                const float t = __fmul_rn(x[e], rs);
+                float q = rintf(t);
+                if (!(fabsf(t - q) <= 0.499969482421875f)) q = rintf(__fdiv_rn(x[e], sc));
+                q = fminf(fmaxf(q, -7.0f), 7.0f);
+                word |= static_cast<uint32_t>(static_cast<int>(q) + 8) << (4 * ((l * VPL + e) & 7));
+            }
+            if constexpr (kF32) {
+                // 4 levels per load: two loads make one word
+                if (l & 1) dst[l >> 1] = prev | word;
+                else prev = word;
+            } else {
+                dst[l] = word;
+            }
+        }
+        p.scales[g] = __float2half_rn(sc);
+        p.zeros[g] = 8;
+    }
+}
+
 __device__ __forceinline__ float candidate(int i, int n, float lo, float hi, float step) {
     if (n == 1) return lo;
     if (i == n - 1) return hi;

@@ -5,6 +5,7 @@
 // enqueue it on the caller's stream with cudaLaunchKernelEx (whose return value is
 // the launch status); they never synchronize and never allocate.
 #include <atomic>
+#include <cmath>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -422,7 +423,8 @@ int quantize_pack_impl(const void *W, int w_dtype, int64_t N, int64_t K, int gro
     return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
 }
 
-// Both calibrated quantizers: validation and the launch (one warp per group).
+// Both calibrated quantizers: validation and the launch (one warp per group; one thread
+// per group for percentiles within 8 of either end of the group).
 int quantize_calib_impl(bool mse, const void *W, int w_dtype, int64_t N, int64_t K, int group, float pct,
                         int candidates, uint8_t *qweight, void *scales, uint8_t *zeros, cudaStream_t stream) {
     if (N < 0 || K < 0 || group <= 0) return W4_ERR_INVALID_ARG;
@@ -454,6 +456,30 @@ int quantize_calib_impl(bool mse, const void *W, int w_dtype, int64_t N, int64_t
     if (mse)
         return f32 ? launch(cb::calib_mse_kernel<true>, grid, block, 0, stream, prm)
                    : launch(cb::calib_mse_kernel<false>, grid, block, 0, stream, prm);
+    // The order statistics the percentile needs (same fp32 arithmetic as the kernels):
+    // within 8 of either end of the group, one thread per group keeps a short sorted list.
+    const float qf = pct / 100.0f;
+    const float h = qf * 127.0f;
+    const int fl = static_cast<int>(std::floor(h));
+    const int lo = fl < 0 ? 0 : (fl > 127 ? 127 : fl);
+    const int hi = lo + 1 < 127 ? lo + 1 : 127;
+    if (lo >= 120 || hi <= 7) {
+        int64_t tblocks = (prm.groups + cb::NUM_THREADS - 1) / cb::NUM_THREADS;
+        if (tblocks > cap) tblocks = cap;
+        const dim3 tgrid(static_cast<unsigned>(tblocks));
+        const bool top = lo >= 120, two = top ? lo >= 126 : hi <= 1;
+        if (top && two)
+            return f32 ? launch(cb::calib_percentile_ends_kernel<true, true, 2>, tgrid, block, 0, stream, prm)
+                       : launch(cb::calib_percentile_ends_kernel<false, true, 2>, tgrid, block, 0, stream, prm);
+        if (top)
+            return f32 ? launch(cb::calib_percentile_ends_kernel<true, true, 8>, tgrid, block, 0, stream, prm)
+                       : launch(cb::calib_percentile_ends_kernel<false, true, 8>, tgrid, block, 0, stream, prm);
+        if (two)
+            return f32 ? launch(cb::calib_percentile_ends_kernel<true, false, 2>, tgrid, block, 0, stream, prm)
+                       : launch(cb::calib_percentile_ends_kernel<false, false, 2>, tgrid, block, 0, stream, prm);
+        return f32 ? launch(cb::calib_percentile_ends_kernel<true, false, 8>, tgrid, block, 0, stream, prm)
+                   : launch(cb::calib_percentile_ends_kernel<false, false, 8>, tgrid, block, 0, stream, prm);
+    }
     return f32 ? launch(cb::calib_percentile_kernel<true>, grid, block, 0, stream, prm)
                : launch(cb::calib_percentile_kernel<false>, grid, block, 0, stream, prm);
 }
