@@ -42,9 +42,12 @@ def assert_calib_equal(env, W, method, param):
         raise AssertionError(f"qweight differs at {len(bad)} bytes, first {bad[:5].tolist()}")
 
 
-@pytest.mark.parametrize("p", [99.9, 50.0, 100.0, 0.5, 12.5])
+@pytest.mark.parametrize("p", [99.9, 50.0, 100.0, 0.5, 12.5, 95.0, 3.0, 99.5, 0.1])
 @pytest.mark.parametrize("dtype", [np.float16, np.float32])
 def test_percentile_random(env, p, dtype):
+    """Order statistics near the top (99.9, 100, 99.5: the two largest; 95: within 8 of the
+    top), near the bottom (0.1, 0.5: the two smallest; 3: within 8) and in the middle
+    (50, 12.5: the sorted path)."""
     import synth
     W, _ = synth.make_random(96, 1024, 1, seed=int(p * 10) + 3, w_dtype="f16")
     assert_calib_equal(env, W.astype(dtype), "percentile", p)
