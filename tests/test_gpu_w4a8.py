@@ -78,7 +78,7 @@ def run_w4a8(env, A_bits, W, M):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 300, 2048), (1, 1031, 4096), (1, 77, 8192), (1, 5000, 16384),
-                                   (2, 37, 4096), (8, 1031, 8192), (16, 200, 4096),
+                                   (2, 37, 4096), (8, 1031, 8192), (16, 200, 4096), (3, 1031, 2048), (8, 300, 4096),
                                    (5, 17, 6144), (12, 2500, 2048)])
 def test_w4a8_decode_path(env, M, N, K):
     """Shapes the decode kernels take, with no workspace: M = 1 on integer dot products

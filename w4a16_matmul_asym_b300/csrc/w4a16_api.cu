@@ -280,7 +280,8 @@ int launch_gemv_mma(const void *A, bool i8, const float *row_scale, int64_t M, i
     const int nb = m <= 8 ? 1 : 2;
     int gpw = 0, stages = 0;
     gm::plan(m, k, &gpw, &stages);
-    const int smem = gm::smem_bytes(m, k, nb, gpw, stages);
+    const bool regb = gm::regb_ok(m, k, gpw);
+    const int smem = gm::smem_bytes(m, k, nb, gpw, stages, regb);
     gm::Params prm;
     prm.A = A;
     prm.qweight = qweight;
@@ -297,10 +298,13 @@ int launch_gemv_mma(const void *A, bool i8, const float *row_scale, int64_t M, i
     const int grid = prm.tiles < sms ? prm.tiles : sms;
     CUtensorMap tmW, tmS, tmZ;
     if (!gm::make_maps(&tmW, &tmS, &tmZ, qweight, scales, zeros, N, K, gpw)) return W4_ERR_CUDA;
-    decltype(&gm::gemv_mma_kernel<1, 1, false>) kern;
-    if (nb == 1 && gpw == 2) kern = i8 ? gm::gemv_mma_kernel<1, 2, true> : gm::gemv_mma_kernel<1, 2, false>;
-    else if (nb == 1) kern = i8 ? gm::gemv_mma_kernel<1, 1, true> : gm::gemv_mma_kernel<1, 1, false>;
-    else kern = i8 ? gm::gemv_mma_kernel<2, 1, true> : gm::gemv_mma_kernel<2, 1, false>;
+    decltype(&gm::gemv_mma_kernel<1, 1, false, false>) kern;
+    if (regb && gpw == 2) kern = i8 ? gm::gemv_mma_kernel<1, 2, true, true> : gm::gemv_mma_kernel<1, 2, false, true>;
+    else if (regb) kern = i8 ? gm::gemv_mma_kernel<1, 1, true, true> : gm::gemv_mma_kernel<1, 1, false, true>;
+    else if (nb == 1 && gpw == 2)
+        kern = i8 ? gm::gemv_mma_kernel<1, 2, true, false> : gm::gemv_mma_kernel<1, 2, false, false>;
+    else if (nb == 1) kern = i8 ? gm::gemv_mma_kernel<1, 1, true, false> : gm::gemv_mma_kernel<1, 1, false, false>;
+    else kern = i8 ? gm::gemv_mma_kernel<2, 1, true, false> : gm::gemv_mma_kernel<2, 1, false, false>;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
     return launch_pdl(kern, dim3(grid), dim3(gm::NUM_THREADS), smem, stream, tmW, tmS, tmZ, prm);
 }
