@@ -68,9 +68,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 CSRC = "w4a16_matmul_asym_b300/csrc/"
 KERNEL_SOURCES = {  # every file a kernel is compiled from (its digest dates a profile)
-    "quantize_pack": [CSRC + "quantize_pack.cuh", CSRC + "common.cuh"],
-    "gemv": [CSRC + "gemv_dp4a.cuh", CSRC + "gemv.cuh", CSRC + "common.cuh"],
-    "gemv_mma": [CSRC + "gemv_mma.cuh", CSRC + "common.cuh"],
+    "quantize_pack": [CSRC + "quantize_pack.cuh", CSRC + "common.cuh", CSRC + "prefetch.cuh"],
+    "gemv": [CSRC + "gemv_dp4a.cuh", CSRC + "gemv.cuh", CSRC + "common.cuh", CSRC + "prefetch.cuh"],
+    "gemv_mma": [CSRC + "gemv_mma.cuh", CSRC + "common.cuh", CSRC + "prefetch.cuh"],
     "quantize_calib": [CSRC + "quantize_calib.cuh", CSRC + "common.cuh"],
     "act_quant": [CSRC + "act_quant.cuh", CSRC + "common.cuh"],
     "gptq": [CSRC + "gptq.cuh", CSRC + "common.cuh"],

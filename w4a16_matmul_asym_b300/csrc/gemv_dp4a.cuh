@@ -47,6 +47,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "prefetch.cuh"
 
 namespace w4 {
 namespace gemv_dp4a {
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) w4a16_gemv_dp4a_kernel(const P
     }
     __syncthreads();
     // On bands of 96 KB or more, the first 32 KB of weights start towards L2 while the
-    // preceding kernel drains (a hint that reads nothing into the CTA, common.cuh).
+    // preceding kernel drains (a hint that reads nothing into the CTA, prefetch.cuh).
     // Measured 7.51 -> 7.06 us on 11008 x 4096 and 9.24 -> 8.74 us on 14336 x 4096; on the
     // 57 KB bands of 4096 x 4096 it cost 5 %, hence the floor.
     if (threadIdx.x == 0 && static_cast<int64_t>(n_end - n_begin) * (p.K / 2) >= 98304)

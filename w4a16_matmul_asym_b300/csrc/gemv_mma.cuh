@@ -46,7 +46,7 @@
 // Launch: with programmatic dependent launch, so the next kernel's launch overlaps this
 // one's tail; every thread waits (griddepcontrol.wait) for the preceding kernel in the
 // stream before reading global memory.  Only an L2 prefetch of the first 64 KB of the
-// CTA's weight band goes out earlier (common.cuh: a hint that reads nothing into the CTA);
+// CTA's weight band goes out earlier (prefetch.cuh: a hint that reads nothing into the CTA);
 // it measured 3-6 % faster on every decode shape tried, e.g. 5.49 -> 5.24 us for M = 8,
 // N = K = 4096 and 31.1 -> 30.4 us for M = 8, 28672 x 8192.
 //
@@ -66,6 +66,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "prefetch.cuh"
 #include "gemm_tcgen05.cuh"   // tensor-map encoding (driver entry point)
 
 namespace w4 {

@@ -420,11 +420,13 @@ int quantize_pack_impl(const void *W, int w_dtype, int64_t N, int64_t K, int gro
     if (w_dtype == W4_DTYPE_F16) {
         auto kern = w4::quantize_pack_kernel<false, kSym>;
         if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
-        return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
+        return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp,
+                          static_cast<const uint8_t *>(W));
     }
     auto kern = w4::quantize_pack_kernel<true, kSym>;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), w4::quant::SMEM_BYTES)) return rc;
-    return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp);
+    return launch_pdl(kern, grid, block, w4::quant::SMEM_BYTES, stream, tmW, total_groups, qw, sc, zeros, wp,
+                      static_cast<const uint8_t *>(W));
 }
 
 // Both calibrated quantizers: validation and the launch (one warp per group; one thread
