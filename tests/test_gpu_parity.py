@@ -427,6 +427,31 @@ def test_matmul_gemm_output_guard(env, M, N, K, offset):
     assert ok, f"worst ratio {worst:.3g} at {idx}"
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 4000, 8192), (4, 300, 4096), (12, 1031, 2048), (64, 300, 1024)])
+def test_matmul_unaligned_tables(env, M, N, K):
+    """Scales and zero points that start one element past a 16-byte boundary (2- and
+    1-byte aligned, which the C ABI accepts).  The streaming kernels copy the tables
+    with tensor copies that need 16-byte alignment, so they step aside (the plain GEMV
+    for M <= 8, the GEMM, which loads its tables directly, above), and the result still
+    matches the oracle."""
+    import synth
+    torch, w4, orc = env
+    W, A = synth.make_random(N, K, M, seed=7 * M + N + K)
+    q, s, z = orc.quantize_pack(W)
+    sbuf = torch.zeros(s.size + 8, dtype=torch.float16, device="cuda")
+    zbuf = torch.zeros(z.size + 16, dtype=torch.uint8, device="cuda")
+    s_d = sbuf[1:1 + s.size].view(s.shape)
+    z_d = zbuf[1:1 + z.size].view(z.shape)
+    s_d.copy_(torch.from_numpy(s))
+    z_d.copy_(torch.from_numpy(z))
+    assert s_d.data_ptr() % 16 == 2 and z_d.data_ptr() % 16 == 1
+    Y = w4.matmul(to_dev_bf16(torch, A), torch.from_numpy(q).cuda(), s_d, z_d)
+    torch.cuda.synchronize()
+    Yref, S = orc.matmul(A, q, s, z)
+    ok, worst, idx = orc.check_y(y_bits(torch, Y), Yref, S)
+    assert ok, f"worst ratio {worst:.3g} at {idx}"
+
+
 @pytest.mark.parametrize("M,N,K", [(512, 38400, 128), (300, 20000, 256)])
 def test_matmul_gemm_many_tiles_full(env, M, N, K):
     """More than twice as many tiles as SMs at small K, every output compared: the
