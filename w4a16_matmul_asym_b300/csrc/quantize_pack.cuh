@@ -29,15 +29,19 @@
 //
 // The quotient w/s without a divide per element: t = w * fl(1/s) lies within 3 ulp
 // of the IEEE quotient x = fl(w/s) (two roundings of 2^-24 relative each, plus x's
-// own).  For |t| <= 64 that is below 2^-16, so whenever t is farther than 2^-16 from
-// a half-integer, rhe(t) == rhe(x) and no tie can occur.  Elements inside that
-// window (about 3e-5 of them) redo the word with the IEEE division __fdiv_rn.
-// Elements with |t| > 31.5 clip to level 0 or 15 whatever integer they round to.
-//   tie test: with M = 1.5 * 2^23, fl(t + M + zp) - (M + zp) = rhe(t) exactly for
-//             |t| < 2^22, so e = t - rhe(t) is exact.
-//   level:    lv = sat((t + zp) / 15) with one fma.sat; outside the tie window the
-//             rounding of fl(15 lv + M) - M is that of t + zp (the fma's errors stay
-//             below 6e-6 < 2^-16) and the saturation performs the clip to [0, 15].
+// own), i.e. within 1.2e-5 for |x| <= 64.  Only x + zp in [-0.5, 15.5] (|x| < 16)
+// escapes the clip, so that bound is the one that matters.
+//   level:    lv = sat((t + zp) / 15) with one fma.sat, which also performs the clip
+//             to [0, 15]; |15 lv - (t + zp)| < 3e-6 below saturation (the roundings
+//             of fl(1/15), of zp fl(1/15) and of the fma, 2^-24 relative each, on
+//             values up to 15.5).  With M = 1.5 * 2^23, q = fl(15 lv + M) = M + rhe(15 lv).
+//   tie test: e = fl(15 lv - (q - M)) is 15 lv minus its rounding, to 2^-25.  When
+//             |e| <= 0.5 - 2^-15, 15 lv is at least 2^-15 = 3.05e-5 from every
+//             half-integer, so x + zp (within 1.2e-5 + 3e-6 of 15 lv) rounds to the
+//             same integer and q is the exact level.  Words with an element outside
+//             that (about 6e-5 of the elements) redo the word with the IEEE division
+//             __fdiv_rn.  A saturated lv gives e = 0: the clipped level needs no
+//             tie-breaking.
 //   packing:  four levels per fp32 lane of an f32x2 pair, 2^23 + q0 + 16 q1 + 256 q2
 //             + 4096 q3 (exact), the two 16-bit sums merged with one prmt.
 #pragma once
@@ -48,7 +52,7 @@
 namespace w4 {
 
 constexpr float kRoundMagic = 12582912.0f;              // 1.5 * 2^23
-constexpr float kHalfMinusSlack = 0.4999847412109375f;  // 0.5 - 2^-16
+constexpr float kTieEdge = 0.499969482421875f;         // 0.5 - 2^-15
 
 // ---- f32x2 helpers (Blackwell packed fp32) ------------------------------------------
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
@@ -149,38 +153,12 @@ __device__ __forceinline__ float level_exact(float w, const GroupParams &p) {
     return fminf(fmaxf(v, kRoundMagic), kRoundMagic + 15.0f);
 }
 
-// 8 consecutive elements w[0..7] -> one 32-bit word of nibbles (element i in bits
-// [4i, 4i+4)).  Pairs are (w[j], w[j+4]) so that one f32x2 packing chain builds the
-// low and the high 16 bits at once.
-__device__ __forceinline__ uint32_t quantize8(const float (&w)[8], const GroupParams &p) {
+// Four f32x2 pairs q[j] = M + level (elements j and j + 4) -> one 32-bit word of
+// nibbles (element i in bits [4i, 4i+4)): one f32x2 packing chain builds the low and
+// the high 16 bits at once; element 0's pair takes M - 2^23 off so the chain carries 2^23.
+__device__ __forceinline__ uint32_t pack8(const uint64_t (&q)[4]) {
     const uint64_t M2 = f2pack(kRoundMagic, kRoundMagic);
     const uint64_t M22 = f2pack(4194304.0f, 4194304.0f);  // 2^22: L - 2^22 = 2^23 + q
-    const uint64_t c15x2 = f2pack(15.0f, 15.0f);
-    uint64_t t[4];
-    bool tie = p.exact;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        t[j] = f2mul(f2pack(w[j], w[j + 4]), p.rcp2);
-        const uint64_t v = f2add(t[j], p.mz2);
-        const uint64_t e = f2sub(t[j], f2sub(v, p.mz2));
-        float elo, ehi;
-        f2unpack(e, elo, ehi);
-        tie |= (fabsf(elo) > kHalfMinusSlack) | (fabsf(ehi) > kHalfMinusSlack);
-    }
-    uint64_t q[4];
-    if (!tie) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float tlo, thi;
-            f2unpack(t[j], tlo, thi);
-            const uint64_t lv = f2pack(fma_sat(tlo, p.r15, p.c15), fma_sat(thi, p.r15, p.c15));
-            q[j] = f2fma(lv, c15x2, M2);            // M + level
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) q[j] = f2pack(level_exact(w[j], p), level_exact(w[j + 4], p));
-    }
-    // q[j] = M + level; element 0 pair takes M - 2^23 off so the chain carries 2^23.
     uint64_t acc = f2sub(q[0], M22);
     acc = f2fma(f2sub(q[1], M2), f2pack(16.0f, 16.0f), acc);
     acc = f2fma(f2sub(q[2], M2), f2pack(256.0f, 256.0f), acc);
@@ -192,6 +170,37 @@ __device__ __forceinline__ uint32_t quantize8(const float (&w)[8], const GroupPa
     return word;
 }
 
+// 8 consecutive elements w[0..7] -> their word by the reciprocal path.  `tie` is set
+// when an element falls in the tie window (or the group has no finite reciprocal):
+// the word must then be redone by quantize8_exact.
+__device__ __forceinline__ uint32_t quantize8_fast(const float (&w)[8], const GroupParams &p, bool &tie) {
+    const uint64_t M2 = f2pack(kRoundMagic, kRoundMagic);
+    const uint64_t c15x2 = f2pack(15.0f, 15.0f);
+    uint64_t q[4];
+    tie = p.exact;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint64_t t = f2mul(f2pack(w[j], w[j + 4]), p.rcp2);
+        float tlo, thi;
+        f2unpack(t, tlo, thi);
+        const uint64_t lv = f2pack(fma_sat(tlo, p.r15, p.c15), fma_sat(thi, p.r15, p.c15));
+        q[j] = f2fma(lv, c15x2, M2);                             // M + level
+        const uint64_t e = f2fma(lv, c15x2, f2sub(M2, q[j]));    // 15 lv - level
+        float elo, ehi;
+        f2unpack(e, elo, ehi);
+        tie |= (fabsf(elo) > kTieEdge) | (fabsf(ehi) > kTieEdge);
+    }
+    return pack8(q);
+}
+
+// The same word with every quotient by IEEE division.
+__device__ __forceinline__ uint32_t quantize8_exact(const float (&w)[8], const GroupParams &p) {
+    uint64_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = f2pack(level_exact(w[j], p), level_exact(w[j + 4], p));
+    return pack8(q);
+}
+
 template <bool kF32>
 struct QuantCfg {
     static constexpr int kLanesPerGroup = kF32 ? 4 : 2;
@@ -200,6 +209,23 @@ struct QuantCfg {
     static constexpr int kLoads = 8;                             // 16-byte loads per lane
     static constexpr int kWords = kElemsPerLane / 8;             // output words per lane
 };
+
+// Elements 8c .. 8c+7 of a lane's 128 bytes of W, widened exactly to fp32.
+template <bool kF32>
+__device__ __forceinline__ void lane_elems(const uint4 (&cur)[QuantCfg<kF32>::kLoads], int c, float (&w)[8]) {
+    if constexpr (kF32) {
+        const float *f = reinterpret_cast<const float *>(cur) + 8 * c;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = f[i];
+    } else {
+        const uint32_t *u = reinterpret_cast<const uint32_t *>(cur) + 4 * c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[2 * i] = widen_lo(u[i]);
+            w[2 * i + 1] = widen_hi(u[i]);
+        }
+    }
+}
 
 // One lane's 128 bytes of W (cur, natural order) -> its qweight words; the group's
 // scale and zero point are written by the lane with part 0.  g = flat group index.
@@ -245,23 +271,16 @@ __device__ __forceinline__ void quantize_lane(const uint4 (&cur)[QuantCfg<kF32>:
     const GroupParams p = group_params<kSym>(mn, mx);
 
     // ---- quantize and pack, 8 elements per output word ----
+    // (Redoing the rare tie-window words in a second loop instead of at once spilled
+    // at the 96-register cap of 17 warps and ran 20 % slower.)
     uint32_t words[C::kWords];
 #pragma unroll
     for (int c = 0; c < C::kWords; ++c) {
         float w[8];
-        if constexpr (kF32) {
-            const float *f = reinterpret_cast<const float *>(cur) + 8 * c;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = f[i];
-        } else {
-            const uint32_t *u = reinterpret_cast<const uint32_t *>(cur) + 4 * c;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                w[2 * i] = widen_lo(u[i]);
-                w[2 * i + 1] = widen_hi(u[i]);
-            }
-        }
-        words[c] = quantize8(w, p);
+        lane_elems<kF32>(cur, c, w);
+        bool tie;
+        words[c] = quantize8_fast(w, p, tie);
+        if (tie) words[c] = quantize8_exact(w, p);
     }
     if (g < total_groups) {
         uint4 *dst = reinterpret_cast<uint4 *>(qw + g * 16 + part * C::kWords);
