@@ -66,6 +66,7 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int DEQ_WARP0 = 12;
 constexpr int NUM_DEQ_WARPS = 8;
 constexpr uint32_t BAR_EPI = 1;               // named barrier of the epilogue warps
+constexpr uint32_t BAR_EPI_RS = 2;            // epilogue warps: the tile's row factors are staged
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;            // accumulator region
 constexpr uint32_t A_COLS = 32;               // one A stage: 64 bf16 per lane
@@ -79,8 +80,13 @@ constexpr int OFF_YST = OFF_W + SW * BQ_STAGE;
 constexpr int OFF_BAR = OFF_YST + NUM_EPI_WARPS * Y_WARP_BYTES;
 constexpr int NUM_BARS = 2 * SA + 2 * SW + 2 * ST + 4 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16;
+// The current tile's per-row factors (W4A8), fp32; 32 spare entries let a chunk of 32
+// columns read past the tile's last column (those columns are never stored).
+constexpr int RS_ENTRIES = MT_MAX + 32;
+constexpr int OFF_RS = OFF_MISC + 16;
+constexpr int SMEM_BYTES = OFF_RS + RS_ENTRIES * 4;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory per CTA");
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 D, bf16 A and B, both
 // K-major, N = mt, M = 128.
@@ -446,15 +452,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // This warp's staging block: `cols` rows of m, 32 consecutive n (64 bytes) each.
         unsigned short *ystage =
             reinterpret_cast<unsigned short *>(smem + OFF_YST + (warp - EPI_WARP0) * Y_WARP_BYTES);
+        float *rs_s = reinterpret_cast<float *>(smem + OFF_RS);
+        const int et = (warp - EPI_WARP0) * 32 + lane;    // 0 .. 255: one tile row factor each
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int mi = tile % m_tiles, ni = tile / m_tiles;
+            // The row factors of the tile's activation rows, one per epilogue thread,
+            // loaded before the accumulator wait so that their latency hides under it.
+            float my_rs = 1.0f;
+            if (p.row_scale != nullptr && et < mt) {
+                const int mr = mi * mt + et;
+                my_rs = __ldg(p.row_scale + (mr < p.M ? mr : p.M - 1));
+            }
             // One warp polls the accumulator barrier; the others sleep on a named barrier
             // and leave the issue slots to the dequantize warps.  The OR of the poller's
             // result gives every warp the same decision.
             uint32_t stop = 0;
             if (warp == EPI_WARP0) stop = warp_wait(&acc_full[acc], acc_phase, abort_flag, tmo) ? 0u : 1u;
             if (named_bar_or(BAR_EPI, NUM_EPI_WARPS * 32, stop)) break;
+            if (p.row_scale != nullptr) {
+                // Every epilogue warp is past the previous tile (barrier above), so the
+                // staged factors can be replaced; the second barrier publishes them.
+                if (et < mt) rs_s[et] = my_rs;
+                asm volatile("bar.sync %0, %1;" ::"n"(BAR_EPI_RS), "n"(NUM_EPI_WARPS * 32) : "memory");
+            }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    acc * 128u + static_cast<uint32_t>(half * cols);
@@ -474,14 +495,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (c0 + 8 * j < cols) tmem_ld_8cols(tbase + c0 + 8 * j, v + 8 * j);
                 tmem_wait_ld();
                 if (p.row_scale != nullptr) {
-                    // Column j of this chunk is activation row m0 + c0 + j: scale it in fp32
-                    // (the same address in every lane: one broadcast load per column).
+                    // Column j of this chunk is activation row m0 + c0 + j, tile row
+                    // half * cols + c0 + j: scale it in fp32 by the staged factor (the same
+                    // shared-memory word in every lane: a broadcast).  Loading the factors
+                    // from global memory here, per chunk, cost 22 us on 2048 x 14336 x 4096.
+                    const float *rsc = rs_s + half * cols + c0;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int mr = m0 + c0 + j;
-                        const float rs = __ldg(p.row_scale + (mr < p.M ? mr : p.M - 1));
-                        v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), rs));
-                    }
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), rsc[j]));
                 }
                 if (c0 + 32 >= cols) {
                     // This warp's part of the accumulator is in registers: hand it back.
