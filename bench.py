@@ -67,7 +67,11 @@ SLEEP_CYCLES = 4_000_000   # ~2 ms sleep kernel ahead of each event window
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 CSRC = "w4a16_matmul_asym_b300/csrc/"
-KERNEL_SOURCES = {  # every file a kernel is compiled from (its digest dates a profile)
+# The files that hold each kernel family's device code: its own header and the device
+# headers it includes.  Their digest dates a profile.  Left out: the public header (error
+# codes only) and gemm_tcgen05.cuh in the warp-MMA family, which takes only its host-side
+# tensor-map helpers from there.
+KERNEL_SOURCES = {
     "quantize_pack": [CSRC + "quantize_pack.cuh", CSRC + "common.cuh", CSRC + "prefetch.cuh"],
     "gemv": [CSRC + "gemv_dp4a.cuh", CSRC + "gemv.cuh", CSRC + "common.cuh", CSRC + "prefetch.cuh"],
     "gemv_mma": [CSRC + "gemv_mma.cuh", CSRC + "common.cuh", CSRC + "prefetch.cuh"],

@@ -94,3 +94,20 @@ def test_kernel_names_have_sources():
         name = bench.matmul_kernel_name(M, K)
         assert name in bench.KERNEL_SOURCES
         assert len(bench.source_digest(name)) == 16
+
+
+def test_kernel_sources_cover_device_includes():
+    """Every csrc header a kernel family's files include is part of that family's
+    digest, so a profile cannot stay 'current' after a change to code the kernel runs.
+    The one documented exception: the warp-MMA family takes only host-side tensor-map
+    helpers from gemm_tcgen05.cuh."""
+    import re
+    host_only = {("gemv_mma", "gemm_tcgen05.cuh")}
+    for family, files in bench.KERNEL_SOURCES.items():
+        names = {os.path.basename(f) for f in files}
+        for f in files:
+            path = os.path.join(bench.ROOT, f)
+            assert os.path.exists(path), path
+            for inc in re.findall(r'#include "([^"]+)"', open(path).read()):
+                if inc.endswith(".cuh") and (family, inc) not in host_only:
+                    assert inc in names, (family, f, inc)
