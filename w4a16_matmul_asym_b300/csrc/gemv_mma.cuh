@@ -24,10 +24,12 @@
 // (128 bytes = 2 groups, row, group pair), box (128, 16, 8 GPW), with 128-byte swizzle,
 // so they land as [pair][row][128 B] with the 16-byte chunk c of row r stored at
 // c ^ (r & 7); the scales and zero points through 2-D maps.  Rows past N are
-// zero-filled by the copy.  Up to MAX_STAGES stages are in flight.  The activations
-// are copied once per CTA into shared memory, permuted so that every B fragment is one
-// conflict-free 16-byte load (int8 activations, for W4A8, are widened to bf16 there:
-// exact, since |a_q| <= 128).
+// zero-filled by the copy.  Up to MAX_STAGES stages are in flight.  When a tile is a
+// single stage and M <= 8, warp w uses the same groups of A in every tile, so each lane
+// loads its B fragments once, straight from global memory into registers (RB).
+// Otherwise the activations are copied once per CTA into shared memory, permuted so
+// that every B fragment is one conflict-free 16-byte load.  Int8 activations (W4A8) are
+// widened to bf16 on the way, exactly, since |a_q| <= 128.
 //
 // Bank conflicts.  The 8 lanes of a quarter warp read MMA rows g and g + 1 (4 chunks
 // each).  MMA row g reads physical row pi(g) = (g >> 1) + 4 (g & 1) of the tile (and
