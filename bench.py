@@ -337,6 +337,40 @@ def oracle_sample_rate(workload: str, budget_s: float, max_rows: int | None = No
     return passes * nbytes / spent / 1e9, desc, spent / passes, nbytes
 
 
+def oracle_prefill_rate(budget_s: float, threads: int, workload: str = "prefill_gemm"):
+    """Time the CPU oracle's fp64 matmul (as it stands) on a compute-bound workload with
+    every host thread busy: each of `threads` threads runs one oracle.matmul call on its
+    own block of R rows of W against all M activation rows (the C call releases the
+    GIL, so the blocks run in parallel).  R is sized so that a thread spends about
+    `budget_s` seconds.  Returns (TFLOP/s, description, threads)."""
+    import concurrent.futures
+    import oracle
+    import synth
+    oracle.build()
+    wl = synth.WORKLOADS[workload]
+    threads = max(1, min(threads, wl.N))
+    probe = min(8, wl.N)
+    Wp, Ap = synth.make_workload(workload, N=probe)
+    qp, sp, zp = oracle.quantize_pack(Wp)
+    t0 = time.perf_counter()
+    oracle.matmul(Ap, qp, sp, zp)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-6)
+    rows = max(1, min(wl.N // threads, int(budget_s / per_row)))
+    W, A = synth.make_workload(workload, N=threads * rows)
+    q, s, z = oracle.quantize_pack(W)
+    M, K = A.shape
+    blocks = [(q[i * rows:(i + 1) * rows], s[i * rows:(i + 1) * rows], z[i * rows:(i + 1) * rows])
+              for i in range(threads)]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        list(pool.map(lambda b: oracle.matmul(A, *b), blocks))
+        wall = time.perf_counter() - t0
+    flops = 2.0 * M * threads * rows * K
+    desc = (f"oracle fp64 matmul of the {workload} workload (M={M}, K={K}) on {threads} x {rows} "
+            f"of its {wl.N} rows of W, one row block per host thread, {threads} threads at once")
+    return flops / wall / 1e12, desc, threads
+
+
 # ---- our arm --------------------------------------------------------------------------
 class PhaseTimer:
     """Times `count` back-to-back launches of one kernel (see the module docstring)."""
@@ -660,6 +694,11 @@ def run_ours(args, ws, rank, local, dist):
         cores, model = host_cpu()
         result["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                   "sample": desc, "host_cores": cores, "cpu_model": model}
+        if args.cpu_prefill_budget > 0:
+            # The compute-bound case on every host core: the context for roofline_tensor.
+            tf, pdesc, used = oracle_prefill_rate(args.cpu_prefill_budget, cores)
+            result["cpu_baseline_tensor"] = {"value": tf, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+                                             "sample": pdesc, "host_cores": cores, "cpu_model": model}
     return result
 
 
@@ -767,6 +806,9 @@ def main(argv=None):
                     help="seconds of CPU time for the oracle baseline")
     ap.add_argument("--cpu-rows", type=int, default=1024,
                     help="rows of W in the oracle baseline sample")
+    ap.add_argument("--cpu-prefill-budget", type=float, default=5.0,
+                    help="seconds per host thread for the all-core oracle matmul on the prefill "
+                         "workload (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="time the step workload only (no other workloads or extra kernels)")

@@ -111,3 +111,11 @@ def test_kernel_sources_cover_device_includes():
             for inc in re.findall(r'#include "([^"]+)"', open(path).read()):
                 if inc.endswith(".cuh") and (family, inc) not in host_only:
                     assert inc in names, (family, f, inc)
+
+
+def test_all_core_oracle_rate_runs_threads_in_parallel_blocks():
+    """The all-core oracle matmul baseline (the compute-bound case) reports a positive
+    rate, the thread count it used and the sample it timed."""
+    tf, desc, used = bench.oracle_prefill_rate(0.05, 2, workload="tiny")
+    assert tf > 0 and used == 2
+    assert "2 threads at once" in desc and "tiny" in desc
