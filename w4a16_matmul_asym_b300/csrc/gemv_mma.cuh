@@ -590,11 +590,18 @@ inline bool make_maps(CUtensorMap *tmW, CUtensorMap *tmS, CUtensorMap *tmZ, cons
 }
 
 // Groups per warp per stage and ring depth for a shape, or 0 stages if it does not fit.
+// The ring keeps about 64 KB of packed weights in flight per SM (2 stages of 32 KB, or 4
+// of 16 KB), which covers an SM's share of the HBM bandwidth-latency product; deeper
+// rings only delay each CTA's first stage.  Measured against the deepest ring that fits
+// (4-5 stages of 32 KB): 9.13 -> 8.56 us at M = 8, 11008 x 4096; 11.07 -> 9.99 us at M = 4,
+// 14336 x 4096; 16.98 -> 16.38 us at M = 8, 28672 x 4096; unchanged at 4096 x 4096 and
+// 28672 x 8192.
 inline void plan(int M, int K, int *gpw, int *stages) {
     const int nb = M <= 8 ? 1 : 2;
     *gpw = (nb == 1 && K % k_per_stage(2) == 0) ? 2 : 1;
+    const int depth = 65536 / slot_w(*gpw) > 2 ? 65536 / slot_w(*gpw) : 2;
     *stages = 0;
-    for (int s = MAX_STAGES; s >= 2; --s)
+    for (int s = depth < MAX_STAGES ? depth : MAX_STAGES; s >= 2; --s)
         if (smem_bytes(M, K, nb, *gpw, s) <= SMEM_LIMIT) {
             *stages = s;
             return;
