@@ -375,9 +375,10 @@ def test_matmul_gemm_shapes(env, M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(9, 37, 2048), (12, 300, 4096), (16, 4096, 4096), (13, 1031, 2048),
                                    (10, 200, 8192), (16, 9, 6144)])
-def test_matmul_skinny_tensor_core(env, M, N, K):
-    """9 <= M <= 16 with few 128-row tiles and K a multiple of 2048: the kernel that
-    splits K across TMEM lanes (8 or 16 parts per row); odd M pads the B operand."""
+def test_matmul_9_to_16_rows(env, M, N, K):
+    """9 <= M <= 16 with few 128-row tiles and K a multiple of 2048: the warp-MMA decode
+    kernel (two 8-column activation blocks, odd M leaving the last column empty) where
+    its activations fit in shared memory, the tcgen05 GEMM otherwise."""
     import synth
     _, _, orc = env
     W, A = synth.make_random(N, K, M, seed=900 + M + N)

@@ -1,6 +1,6 @@
 """Failure detection without a GPU fault: the consumers of the tensor-core GEMM
-(M = 64), of the split-K tensor-core kernel (M = 12), of the integer-dot decode GEMV
-(M = 1), of the streaming GEMV with activations in shared memory (M = 3) and of the
+(M = 64), of the integer-dot decode GEMV (M = 1), of the warp-MMA decode kernel with
+its activations in registers (M = 3) and in shared memory (M = 12), and of the
 quantize kernel are made
 to wait on a barrier that nothing signals; the bounded wait must run out, record
 W4_ERR_TIMEOUT in the device error word, drain its copies, free tensor memory and

@@ -17,7 +17,6 @@
 #include "gemv.cuh"
 #include "gemv_dp4a.cuh"
 #include "gemv_mma.cuh"
-#include "gemv_tc.cuh"
 #include "gptq.cuh"
 #include "quantize_calib.cuh"
 #include "quantize_pack.cuh"
@@ -208,52 +207,6 @@ int launch_gemv_dp4a(const void *A, bool i8, const float *row_scale, int64_t N, 
                        : (i8 ? gd::w4a16_gemv_dp4a_kernel<2, true> : gd::w4a16_gemv_dp4a_kernel<2, false>);
     if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem)) return rc;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(gd::NUM_THREADS), smem, stream, prm);
-}
-
-// 2 <= M <= 16 on the tensor cores: K a multiple of 2048, the activations (M x K bf16)
-// resident in shared memory, 16-byte aligned scales and zero points.  Returns
-// W4_ERR_UNSUPPORTED for other shapes.
-int launch_skinny_tc(const __nv_bfloat16 *A, int64_t M, int64_t N, int64_t K, const uint8_t *qweight,
-                     const __half *scales, const uint8_t *zeros, __nv_bfloat16 *Y, cudaStream_t stream,
-                     int sms, w4::WaitParams wp) {
-    namespace gt = w4::gemv_tc;
-    const int P = gt::parts_for(K, M);
-    if (M < 2 || M > gt::MT_MAX || P == 0 || !aligned(scales, 16) || !aligned(zeros, 16) ||
-        N > INT32_MAX / 2 || K > 65536)
-        return W4_ERR_UNSUPPORTED;
-    const int k = static_cast<int>(K);
-    const int MT = P == 16 ? static_cast<int>(M) : static_cast<int>((M + 1) & ~1);  // MT * P % 16 == 0
-    const int NBr = MT * P;
-    if (NBr > 256 || gt::b_bytes(k, MT) > gt::B_MAX_BYTES) return W4_ERR_UNSUPPORTED;
-    int stages = 0;
-    for (int s = gt::MAX_STAGES; s >= 2; --s)
-        if (gt::smem_bytes(k, P, MT, s) <= gt::SMEM_LIMIT) {
-            stages = s;
-            break;
-        }
-    if (stages == 0) return W4_ERR_UNSUPPORTED;
-    int nset = static_cast<int>(gt::ACC_REGION) / NBr;
-    if (nset > gt::MAX_SETS) nset = gt::MAX_SETS;
-    const int smem = gt::smem_bytes(k, P, MT, stages);
-    const int R = 128 / P;
-    gt::Params prm;
-    prm.A = A;
-    prm.qweight = qweight;
-    prm.scales = scales;
-    prm.zeros = zeros;
-    prm.Y = Y;
-    prm.M = static_cast<int>(M);
-    prm.N = static_cast<int>(N);
-    prm.K = k;
-    prm.MT = MT;
-    prm.P = P;
-    prm.stages = stages;
-    prm.nset = nset;
-    prm.tiles = static_cast<int>((N + R - 1) / R);
-    prm.wait = wp;
-    const int grid = prm.tiles < sms ? prm.tiles : sms;
-    if (int rc = ensure_smem_attr(reinterpret_cast<const void *>(gt::w4a16_skinny_tc_kernel), smem)) return rc;
-    return launch(gt::w4a16_skinny_tc_kernel, dim3(grid), dim3(gt::NUM_THREADS), smem, stream, prm);
 }
 
 // 1 <= M <= 16 on warp-level tensor-core MMAs with the weights dequantized in
@@ -581,14 +534,6 @@ int w4_matmul(const void *A, int64_t M, int64_t N, int64_t K, int group, const u
     if (M >= 2 && M <= 16) {
         const int rc = launch_gemv_mma(a, false, nullptr, M, N, K, qweight, s, zeros, y, stream, sms, wait_params(),
                                        false);
-        if (rc != W4_ERR_UNSUPPORTED) return rc;
-    }
-    // 9 <= M <= 16 with few 128-row tiles: the GEMM would leave SMs idle, while the
-    // split-K-in-TMEM kernel spreads 8- or 16-row tiles over all of them.  (For M <= 8
-    // the CUDA-core kernels are faster: measured 14.2 against 18.5 us for M = 8,
-    // N = K = 4096, the split-K kernel being bound by its per-tile fixed costs.)
-    if (M >= 9 && M <= 16 && (N + 127) / 128 < static_cast<int64_t>(sms) * 3 / 4) {
-        const int rc = launch_skinny_tc(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
         if (rc != W4_ERR_UNSUPPORTED) return rc;
     }
     if (M <= 8) return launch_gemv(a, M, N, K, qweight, s, zeros, y, stream, sms, wait_params());
