@@ -251,12 +251,11 @@ W4_API int w4_dequantize(const uint8_t *qweight, const void *scales, const uint8
  *     |Y - Y_exact| <= 8e-3 * sum_k |A[m,k] * W_hat[n,k]| + ulp_bf16(|Y_exact|) / 2.
  * Paths: M = 1 runs integer dot products (dp4a) on exact block-floating-point
  * activation digits; 2 <= M <= 16 warp-level tensor-core MMAs (bf16 x bf16 -> fp32)
- * on weights dequantized in registers, when K is a multiple of 2048 and the activations
- * fit in shared memory; otherwise 9 <= M <= 16 with fewer 128-row tiles than three
- * quarters of the SMs a tcgen05 kernel that splits K across tensor-memory lanes, and
- * larger M a tcgen05 tensor-core GEMM (bf16 x bf16 -> fp32 in tensor memory) on weight
- * tiles dequantized into tensor memory.  Shapes a fast path cannot take (K not a
- * multiple of 2048, unaligned scale or zero tables) run a plain CUDA-core kernel.
+ * on weights dequantized in registers, when K is a multiple of 2048, the scale and zero
+ * tables are 16-byte aligned and the activations fit in shared memory; M >= 9 otherwise
+ * a tcgen05 tensor-core GEMM (bf16 x bf16 -> fp32 in tensor memory) on weight tiles
+ * dequantized into tensor memory.  M <= 8 shapes those paths cannot take (K not a
+ * multiple of 2048, unaligned tables, activations too large) run a CUDA-core GEMV.
  *
  * Arguments:
  *   A        device pointer, bf16 [M, K]; 16-byte aligned.
